@@ -72,6 +72,8 @@ class Oracle:
         lib.oracle_fwd.restype = I
         lib.oracle_bwd.argtypes = [dp, dp, dp, dp, L, L, L, D, I, dp, dp, dp]
         lib.oracle_bwd.restype = I
+        lib.oracle_bwd_rows.argtypes = [dp, dp, dp, dp, L, L, L, D, I, lp, L, dp, dp, dp]
+        lib.oracle_bwd_rows.restype = I
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = I
         self._lib = lib
@@ -127,6 +129,26 @@ class Oracle:
             raise RuntimeError(f"oracle_bwd failed ({rc})")
         return dq, dk, dv
 
+    def attention_bwd_rows(self, q, k, v, dout, scale: float, causal: bool, rows):
+        """Backward restricted to the listed query rows of every head.
+
+        Returns (dQ of those rows [B,H,R,d], and the contributions of exactly those
+        rows to dK and dV [B,H,N,d]).  With every row listed this is attention_bwd.
+        """
+        q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+        B, H, N, d = _shape4(q, k, v, dout)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        R = rows.shape[0]
+        dq = np.empty((B, H, R, d))
+        dk = np.empty((B, H, N, d))
+        dv = np.empty((B, H, N, d))
+        rc = self._lib.oracle_bwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B * H, N, d,
+                                       float(scale), int(bool(causal)),
+                                       _ptr(rows, ctypes.c_long), R, _ptr(dq), _ptr(dk), _ptr(dv))
+        if rc:
+            raise RuntimeError(f"oracle_bwd_rows failed ({rc})")
+        return dq, dk, dv
+
 
 def default() -> Oracle:
     """The oracle built from fa_oracle.c (compiled on first use)."""
@@ -151,3 +173,7 @@ def attention_fwd_rows(q, k, v, scale: float, causal: bool, rows):
 
 def attention_bwd(q, k, v, dout, scale: float, causal: bool):
     return default().attention_bwd(q, k, v, dout, scale, causal)
+
+
+def attention_bwd_rows(q, k, v, dout, scale: float, causal: bool, rows):
+    return default().attention_bwd_rows(q, k, v, dout, scale, causal, rows)

@@ -137,15 +137,21 @@ int oracle_fwd(const double *q, const double *k, const double *v, long bh, long 
 }
 
 /*
- * Backward for every head: given dO, the gradients of sum(O o dO) with respect
- * to Q, K and V.  O and the softmax are recomputed here from the definition.
- * Heads run in parallel; inside a head the rows run in order, because dK and dV
- * sum over rows.
+ * Backward restricted to the query rows rows[0..nrows) of every head (rows == NULL:
+ * every row, nrows == n).  dq_rows [B*H, nrows, d] receives dQ of the listed rows;
+ * dk and dv [B*H, n, d] receive the contributions of exactly the listed rows
+ * (sum over i in rows of scale*dS_ij*Q_i and P_ij*dO_i).  With every row listed the
+ * result is the full gradient of sum(O o dO) with respect to Q, K and V.  O and the
+ * softmax are recomputed here from the definition.  Heads run in parallel; inside a
+ * head the rows run in order, because dK and dV sum over rows.
  */
-int oracle_bwd(const double *q, const double *k, const double *v, const double *dout,
-               long bh, long n, long d, double scale, int causal, double *dq, double *dk,
-               double *dv) {
-    if (bh < 0 || n < 0 || d <= 0) return 1;
+int oracle_bwd_rows(const double *q, const double *k, const double *v, const double *dout,
+                    long bh, long n, long d, double scale, int causal, const long *rows,
+                    long nrows, double *dq_rows, double *dk, double *dv) {
+    if (bh < 0 || n < 0 || d <= 0 || nrows < 0) return 1;
+    if (rows == NULL && nrows != n) return 1;
+    for (long r = 0; rows && r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= n) return 1;
     int failed = 0;
 #pragma omp parallel
     {
@@ -162,10 +168,11 @@ int oracle_bwd(const double *q, const double *k, const double *v, const double *
             if (!p || !dp || !oi) continue;
             const double *qh = q + h * n * d, *kh = k + h * n * d, *vh = v + h * n * d;
             const double *doh = dout + h * n * d;
-            double *dqh = dq + h * n * d, *dkh = dk + h * n * d, *dvh = dv + h * n * d;
+            double *dqh = dq_rows + h * nrows * d, *dkh = dk + h * n * d, *dvh = dv + h * n * d;
             memset(dkh, 0, sizeof(double) * (size_t)(n * d));
             memset(dvh, 0, sizeof(double) * (size_t)(n * d));
-            for (long i = 0; i < n; ++i) {
+            for (long r = 0; r < nrows; ++r) {
+                long i = rows ? rows[r] : r;
                 const double *qi = qh + i * d, *doi = doh + i * d;
                 double lse_i;
                 long nk = softmax_row(qi, kh, i, n, d, scale, causal, p, &lse_i);
@@ -181,7 +188,7 @@ int oracle_bwd(const double *q, const double *k, const double *v, const double *
                     dp[j] = p[j] * (s - di);
                 }
                 /* dQ_i = scale * sum_j dS_ij K_j */
-                double *dqi = dqh + i * d;
+                double *dqi = dqh + r * d;
                 for (long t = 0; t < d; ++t) dqi[t] = 0.0;
                 for (long j = 0; j < nk; ++j) {
                     const double *kj = kh + j * d;
@@ -204,4 +211,11 @@ int oracle_bwd(const double *q, const double *k, const double *v, const double *
         free(oi);
     }
     return failed ? 2 : 0;
+}
+
+/* Backward for every head: the gradients of sum(O o dO) with respect to Q, K, V. */
+int oracle_bwd(const double *q, const double *k, const double *v, const double *dout,
+               long bh, long n, long d, double scale, int causal, double *dq, double *dk,
+               double *dv) {
+    return oracle_bwd_rows(q, k, v, dout, bh, n, d, scale, causal, NULL, n, dq, dk, dv);
 }

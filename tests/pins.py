@@ -285,6 +285,26 @@ def pin_sampled_rows_match_full(orc):
         _close(l_r, l[:, :, rows], 0.0, f"sampled rows L (causal={causal})")
 
 
+def pin_sampled_backward_rows(orc):
+    """The row-sampled backward: all rows listed gives the full gradients, and the
+    dK/dV contributions of disjoint row sets add up."""
+    rng = np.random.default_rng(19)
+    q, k, v, do = (rng.standard_normal((1, 2, 21, 5)) for _ in range(4))
+    all_rows = np.arange(21)
+    a, b = np.array([0, 3, 7, 20]), np.array([1, 2, 4, 5, 6] + list(range(8, 20)))
+    for causal in (False, True):
+        dq, dk, dv = orc.attention_bwd(q, k, v, do, 0.4, causal)
+        dq_r, dk_r, dv_r = orc.attention_bwd_rows(q, k, v, do, 0.4, causal, all_rows)
+        _close(dq_r, dq, 0.0, "row-sampled dQ, all rows")
+        _close(dk_r, dk, 0.0, "row-sampled dK, all rows")
+        _close(dv_r, dv, 0.0, "row-sampled dV, all rows")
+        dq_a, dk_a, dv_a = orc.attention_bwd_rows(q, k, v, do, 0.4, causal, a)
+        dq_b, dk_b, dv_b = orc.attention_bwd_rows(q, k, v, do, 0.4, causal, b)
+        _close(dq_a, dq[:, :, a], 0.0, "row-sampled dQ rows")
+        _close(dk_a + dk_b, dk, 1e-13, "dK contributions add up")
+        _close(dv_a + dv_b, dv, 1e-13, "dV contributions add up")
+
+
 ALL_PINS = [
     pin_worked_example_output,
     pin_worked_example_probabilities,
@@ -300,4 +320,5 @@ ALL_PINS = [
     pin_finite_differences,
     pin_page_tiled_case,
     pin_sampled_rows_match_full,
+    pin_sampled_backward_rows,
 ]
