@@ -1,0 +1,321 @@
+#!/usr/bin/env python
+"""Benchmark of exact attention on GB300: one step = forward + backward of causal
+bf16 attention, B=2 H=32 N=8192 d=128, through the library's C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  ``value`` is attention TFLOP/s over the whole step
+(forward 4 N^2 d per head halved for causal, backward 2.5x forward), inputs
+resident in device memory, L2 flushed between steps (untimed), CUDA events on the
+launching stream.  ``--impl reference`` times the fp64 CPU oracle on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOPS (fwd, fwd+bwd) bf16 N=8k d=128 causal; % of GB300 tensor peak"
+WORKLOAD_ID = 3      # B=2 H=32 N=8192 d=128 causal, bf16
+CAUSAL = True
+L2_FLUSH_BYTES = 256 << 20
+CPU_SAMPLE_ROWS = 256   # query rows per head timed on the host for cpu_baseline
+REF_STEP_ROWS = 32      # query rows per head per step of the reference arm
+
+
+def flops_fwd_rows(rows, d, heads, causal=True, n=None):
+    """Forward FLOPs of the listed query rows: 4 d (visible keys) per row."""
+    if causal:
+        keys = sum(int(r) + 1 for r in rows)
+    else:
+        keys = len(rows) * n
+    return 4.0 * d * keys * heads
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), \
+            float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = list(csv.reader(io.StringIO(open(self.path).read())))
+        os.unlink(self.path)
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup(backend):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def cpu_oracle_sample(q, k, v, do, d, rows):
+    """Time the fp64 oracle (forward + backward) on the listed query rows of every head."""
+    import oracle
+    from exact_attention_tmem_gb300 import inputs
+    q64, k64, v64, do64 = (inputs.as_f64(t) for t in (q, k, v, do))
+    scale = 1.0 / math.sqrt(d)
+    heads = q.shape[0] * q.shape[1]
+    t0 = time.perf_counter()
+    oracle.attention_fwd_rows(q64, k64, v64, scale, CAUSAL, rows)
+    oracle.attention_bwd_rows(q64, k64, v64, do64, scale, CAUSAL, rows)
+    dt = time.perf_counter() - t0
+    fl = 3.5 * flops_fwd_rows(rows, d, heads, CAUSAL)
+    return fl / dt / 1e12, dt, oracle.num_threads()
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle, as it stands, on sampled rows."""
+    if rank != 0:
+        return
+    from exact_attention_tmem_gb300 import inputs
+    w = inputs.WORKLOADS[WORKLOAD_ID]
+    q, k, v, do = inputs.workload_inputs(WORKLOAD_ID, with_grad_out=True)
+    times, cores, fl = [], 1, 0.0
+    for step in range(args.warmup + args.steps):
+        rows = inputs.sample_rows(w.N, REF_STEP_ROWS, seed=100 + step)
+        tf, dt, cores = cpu_oracle_sample(q, k, v, do, w.d, rows)
+        if step >= args.warmup:
+            times.append(dt)
+            fl += 3.5 * flops_fwd_rows(rows, w.d, w.B * w.H, CAUSAL)
+    value = fl / sum(times) / 1e12
+    sample = (f"{REF_STEP_ROWS} seeded query rows of each of the {w.B * w.H} heads per step "
+              "(forward + backward of those rows, fp64)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w):
+    return {"workload": f"fwd+bwd causal bf16 B={w.B} H={w.H} N={w.N} d={w.d}",
+            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": CAUSAL, "scale": "1/sqrt(d)",
+            "inputs": "iid N(0,1) rounded to bf16, seeds 3001-3004",
+            "l2": "inputs 512 MiB > L2; L2 flushed (256 MiB write) between timed steps",
+            "parallelism": "one independent replica per GPU"}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import exact_attention_tmem_gb300 as fa
+    from exact_attention_tmem_gb300 import inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.build()
+    w = inputs.WORKLOADS[WORKLOAD_ID]
+    B, H, N, d = w.B, w.H, w.N, w.d
+    scale = 1.0 / math.sqrt(d)
+    q_h, k_h, v_h, do_h = inputs.workload_inputs(WORKLOAD_ID, with_grad_out=True)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fwd(q, k, v, causal=CAUSAL, scale=scale, out=o, lse=lse)
+        fa.bwd(q, k, v, o, lse, do, causal=CAUSAL, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    if fa.device_status() != 0:
+        raise RuntimeError("device status reports a timed-out wait during warm-up")
+
+    fwd_flops = w.fwd_flops(CAUSAL)
+    bwd_flops = 2.5 * fwd_flops
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fa.fwd(q, k, v, causal=CAUSAL, scale=scale, out=o, lse=lse)
+            ev[i][1].record(stream)
+            fa.bwd(q, k, v, o, lse, do, causal=CAUSAL, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    status = fa.device_status()
+    t_fwd = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    t_bwd = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    t_step = [a + b for a, b in zip(t_fwd, t_bwd)]
+    total_ms = sum(t_step)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * args.steps * (fwd_flops + bwd_flops) / (total_ms * 1e-3) / 1e12
+    fwd_tf = fwd_flops / (statistics.mean(t_fwd) * 1e-3) / 1e12
+    bwd_tf = bwd_flops / (statistics.mean(t_bwd) * 1e-3) / 1e12
+
+    # ---- end to end through the public API: pinned host inputs in, results back out
+    hq, hk, hv, hdo = (t.pin_memory() for t in (q_h, k_h, v_h, do_h))
+    ho, hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (q_h, q_h, k_h, v_h))
+    hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+
+    def e2e_step():
+        for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_value = world * (fwd_flops + bwd_flops) / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+    peak_burst, peak_sust, hbm, peak_src = peaks()
+    dominant = "bwd" if statistics.mean(t_bwd) >= statistics.mean(t_fwd) else "fwd"
+    dom_tf = bwd_tf if dominant == "bwd" else fwd_tf
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(w),
+        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+        "fwd_ms": statistics.mean(t_fwd), "bwd_ms": statistics.mean(t_bwd),
+        "fwd_frac_of_peak": fwd_tf / peak_burst, "bwd_frac_of_peak": bwd_tf / peak_burst,
+        "roofline": {"bound": "tensor", "kernel": f"{dominant} (CUDA events around the C-ABI call)",
+                     "achieved": dom_tf, "peak": peak_burst, "unit": "TFLOP/s",
+                     "frac": dom_tf / peak_burst, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 burst"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "device_status": status,
+    }
+    clocks = clk.summary()
+    line["clocks"] = clocks
+    if world == 1 and not args.no_cpu_baseline:
+        rows = inputs.sample_rows(N, CPU_SAMPLE_ROWS, seed=7)
+        tf, dt, cores = cpu_oracle_sample(q_h, k_h, v_h, do_h, d, rows)
+        line["cpu_baseline"] = {
+            "value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": (f"{len(rows)} seeded query rows of each of the {B * H} heads, forward + "
+                       f"backward of those rows in fp64, {dt:.1f} s")}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip timing the fp64 oracle on the host")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        world, rank, _ = dist_setup("gloo")
+        run_reference(args, world, rank)
+    else:
+        world, rank, local = dist_setup("nccl")
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,105 @@
+"""Exact softmax attention for GB300 (sm_103a): forward and backward.
+
+    o, lse = fwd(q, k, v, causal=True)            # q, k, v: [B, H, N, d] CUDA tensors
+    dq, dk, dv = bwd(q, k, v, o, lse, do, causal=True)
+
+The arithmetic runs in hand-written tcgen05/TMA kernels inside libfa_gb300.so,
+reached through its C ABI (include/fa.h).  PyTorch provides device memory and
+streams only.  ``build()`` compiles the library in-tree with nvcc.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+from ._lib import FaError  # noqa: F401
+
+__all__ = ["fwd", "bwd", "bwd_workspace_size", "device_status", "build", "FaError"]
+
+
+def build(force: bool = False) -> str:
+    from .buildlib import build as _build
+    return _build(force=force)
+
+
+def _stream_ptr(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check_qkv(dtype, *ts):
+    t0 = ts[0]
+    if t0.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+        if t.dtype != dtype:
+            raise ValueError(f"expected {dtype}, got {t.dtype}")
+        if t.shape != t0.shape:
+            raise ValueError("q, k, v (and o, dO) must share one [B, H, N, d] shape")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        if t.device != t0.device:
+            raise ValueError("tensors must be on one device")
+
+
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
+    """O = softmax(scale * q k^T [causal mask]) v and the natural-log logsumexp per row.
+
+    bf16 tensors use fa_fwd; float32 tensors use fa_fwd_f32 (d = 64 only).
+    Returns (o, lse) with lse float32 [B, H, N].
+    """
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q, k, v must be bfloat16 or float32")
+    _check_qkv(dtype, q, k, v)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_qkv(dtype, q, out)
+    if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    lib = _lib.load()
+    fn = lib.fa_fwd if dtype == torch.bfloat16 else lib.fa_fwd_f32
+    st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+            B, H, N, d, scale, int(bool(causal)), _stream_ptr(q.device))
+    _lib.check(st, "fa_fwd" if dtype == torch.bfloat16 else "fa_fwd_f32")
+    return out, lse
+
+
+def bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(_lib.load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
+        dq=None, dk=None, dv=None, workspace=None):
+    """Gradients (dq, dk, dv) of sum(o * do), recomputing the probabilities from lse."""
+    _check_qkv(torch.bfloat16, q, k, v, o, do)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_qkv(torch.bfloat16, q, dq, dk, dv)
+    if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    need = bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = _lib.load().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            B, H, N, d, scale, int(bool(causal)), _stream_ptr(q.device))
+    _lib.check(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(_lib.load().fa_get_device_status(s.cuda_stream))

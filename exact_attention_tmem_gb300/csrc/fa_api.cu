@@ -1,0 +1,262 @@
+// fa_api.cu — the C ABI declared in include/fa.h: argument checks, tensor-map
+// encoding, the device status word, and dispatch to the kernel launchers.
+//
+// Every check that needs no GPU runs first, so that argument errors are reported
+// identically on a machine without one.  Nothing here allocates device memory
+// or synchronises a stream (fa_get_device_status excepted, by contract).
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+// The device status word.  One copy per device (module-scope variable); kernels
+// receive its address.
+__device__ unsigned int g_status_word[2];
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return FA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Shape checks shared by every entry point.  Products are formed in 64 bits.
+int check_shape(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    const long long bh = static_cast<long long>(B) * H;
+    if (bh > INT_MAX) return FA_ERR_INVALID_ARG;
+    const long long elems = bh * N;
+    if (elems > (1LL << 62) / d) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+// ---- per-device state: the status word's address and the compute capability ----
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+    bool ready = false;
+    bool supported = false;
+    unsigned int *status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_state(DeviceState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceState &s = g_dev[dev];
+    if (!s.ready) {
+        int major = 0, minor = 0;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        s.supported = (major == 10 && minor == 3);
+        if (s.supported) {
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_status_word);
+            if (e != cudaSuccess) return cuda_fail(e);
+            s.status = static_cast<unsigned int *>(p);
+        }
+        s.ready = true;
+    }
+    if (!s.supported) return FA_ERR_UNSUPPORTED;
+    *out = &s;
+    return FA_OK;
+}
+
+// ---- tensor maps ----
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int get_encoder(EncodeTiledFn *fn) {
+    static EncodeTiledFn cached = nullptr;
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (err == cudaSuccess && q != cudaDriverEntryPointSuccess) err = cudaErrorSymbolNotFound;
+        if (err == cudaSuccess) cached = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (cached == nullptr) return cuda_fail(err != cudaSuccess ? err : cudaErrorSymbolNotFound);
+    *fn = cached;
+    return FA_OK;
+}
+
+// [BH, N, d] viewed as 3-D: d innermost, then N, then BH.  One box is 128 bytes of a
+// row by 128 rows, 128-byte swizzled (the layout the MMA descriptors expect).
+int make_tmap(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int eb, int d, int N, int BH) {
+    EncodeTiledFn enc;
+    int st = get_encoder(&enc);
+    if (st != FA_OK) return st;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * eb, static_cast<cuuint64_t>(d) * eb * N};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBoxBytes / eb), static_cast<cuuint32_t>(kTileRows), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return FA_OK;
+}
+
+int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
+               int d, float scale, int causal, cudaStream_t stream, bool f32) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    int st = check_shape(B, H, N, d);
+    if (st != FA_OK) return st;
+    if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (f32 && d != 64) return FA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse))
+        return FA_ERR_ALIGNMENT;
+    DeviceState *ds = nullptr;
+    st = device_state(&ds);
+    if (st != FA_OK) return st;
+    FwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const CUtensorMapDataType dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int eb = f32 ? 4 : 2;
+    const int BH = B * H;
+    if ((st = make_tmap(&a.tm_q, q, dt, eb, d, N, BH)) != FA_OK) return st;
+    if ((st = make_tmap(&a.tm_k, k, dt, eb, d, N, BH)) != FA_OK) return st;
+    if ((st = make_tmap(&a.tm_v, v, dt, eb, d, N, BH)) != FA_OK) return st;
+    a.o = o;
+    a.lse = lse;
+    a.N = N;
+    a.BH = BH;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.status = ds->status;
+    cudaError_t e = f32 ? launch_fwd_f32(a, stream) : launch_fwd_bf16(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
+                      int d, float scale, int causal, fa_stream_t stream) {
+    return fwd_common(q, k, v, o, lse, B, H, N, d, scale, causal, reinterpret_cast<cudaStream_t>(stream),
+                      false);
+}
+
+extern "C" int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse, int B, int H,
+                          int N, int d, float scale, int causal, fa_stream_t stream) {
+    return fwd_common(q, k, v, o, lse, B, H, N, d, scale, causal, reinterpret_cast<cudaStream_t>(stream),
+                      true);
+}
+
+extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+    if (check_shape(B, H, N, d) != FA_OK) return 0;
+    const size_t bh = static_cast<size_t>(B) * H;
+    const size_t npad = (static_cast<size_t>(N) + kTileRows - 1) / kTileRows * kTileRows;
+    const size_t acc = bh * static_cast<size_t>(N) * d * sizeof(float);
+    const size_t acc_aligned = (acc + 255) / 256 * 256;
+    const size_t vec = (bh * npad * sizeof(float) + 255) / 256 * 256;
+    return acc_aligned + 2 * vec;
+}
+
+extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                      const void *dout, void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                      int B, int H, int N, int d, float scale, int causal, fa_stream_t stream) {
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    int st = check_shape(B, H, N, d);
+    if (st != FA_OK) return st;
+    if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
+        !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return FA_ERR_ALIGNMENT;
+    const size_t need = fa_bwd_workspace_size(B, H, N, d);
+    if (workspace == nullptr || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGNMENT;
+    DeviceState *ds = nullptr;
+    st = device_state(&ds);
+    if (st != FA_OK) return st;
+    BwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const int BH = B * H;
+    const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if ((st = make_tmap(&a.tm_q, q, dt, 2, d, N, BH)) != FA_OK) return st;
+    if ((st = make_tmap(&a.tm_k, k, dt, 2, d, N, BH)) != FA_OK) return st;
+    if ((st = make_tmap(&a.tm_v, v, dt, 2, d, N, BH)) != FA_OK) return st;
+    if ((st = make_tmap(&a.tm_do, dout, dt, 2, d, N, BH)) != FA_OK) return st;
+    const size_t npad = (static_cast<size_t>(N) + kTileRows - 1) / kTileRows * kTileRows;
+    const size_t acc = static_cast<size_t>(BH) * N * d * sizeof(float);
+    const size_t acc_aligned = (acc + 255) / 256 * 256;
+    const size_t vec = (static_cast<size_t>(BH) * npad * sizeof(float) + 255) / 256 * 256;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dq_acc = reinterpret_cast<float *>(ws);
+    a.delta = reinterpret_cast<float *>(ws + acc_aligned);
+    a.lse2 = reinterpret_cast<float *>(ws + acc_aligned + vec);
+    a.N = N;
+    a.Npad = static_cast<int>(npad);
+    a.BH = BH;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.status = ds->status;
+    cudaError_t e = launch_bwd_bf16(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
+extern "C" int fa_get_device_status(fa_stream_t stream) {
+    DeviceState *ds = nullptr;
+    int st = device_state(&ds);
+    if (st != FA_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int words[2] = {0, 0};
+    e = cudaMemcpyFromSymbol(words, g_status_word, sizeof(words));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (words[0] != 0) {
+        const unsigned int zero[2] = {0, 0};
+        e = cudaMemcpyToSymbol(g_status_word, zero, sizeof(zero));
+        if (e != cudaSuccess) return cuda_fail(e);
+        return FA_ERR_DEVICE_TIMEOUT;
+    }
+    return FA_OK;
+}
+
+extern "C" const char *fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "ok";
+        case FA_ERR_INVALID_ARG: return "invalid argument (null pointer, size < 1, size overflow or non-finite scale)";
+        case FA_ERR_UNSUPPORTED: return "unsupported (head dim, dtype or device compute capability)";
+        case FA_ERR_ALIGNMENT: return "pointer not aligned (16 bytes for tensors, 4 for lse, 256 for workspace)";
+        case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_bwd_workspace_size()";
+        case FA_ERR_CUDA: return "CUDA call failed (see fa_last_cuda_error)";
+        case FA_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out; outputs are undefined";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int fa_last_cuda_error(void) { return t_last_cuda_error; }

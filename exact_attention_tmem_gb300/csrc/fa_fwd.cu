@@ -1,0 +1,422 @@
+// fa_fwd.cu — forward pass of exact attention on sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes ("FlashAttention" deep dive, section "How it works"): for each
+// query tile Q_i and each key/value tile K_j, V_j in turn, S = Q_i K_j^T * scale,
+// m_new = max(m, rowmax S), P = exp(S - m_new), alpha = exp(m - m_new),
+// l = alpha*l + rowsum P, acc = alpha*acc + P V_j; at the end O_i = acc / l and
+// L_i = m + log l.  Causal tiles above the diagonal are never loaded or multiplied
+// ("tm_flash_attention_arch_2k", section "The architecture: every step explained";
+// deep dive, section "Implementation notes"), and only the diagonal tile is masked.
+//
+// GB300 design (differs from the pages' A100/H100 kernels):
+//  * One CTA owns two 128-row query tiles of one (batch, head) and streams K/V
+//    tiles through a multi-stage shared-memory ring filled by TMA.
+//  * Both contractions run on the 5th-generation tensor cores: S_t = Q_t K_j^T with
+//    both operands in shared memory, O_t += P_t V_j with P_t read from tensor
+//    memory, where the softmax warps wrote it over S_t.  S and O live in tensor
+//    memory (TMEM): S0 | S1 | O0 | O1 = 128 + 128 + d + d of its 512 columns.
+//  * Warp roles: warps 0-3 and 4-7 are the softmax warpgroups of tile 0 and tile 1
+//    (thread r owns row r: tcgen05.ld gives it its whole row, so row max and row
+//    sum need no shuffles); warp 8 issues every MMA from one thread; warp 9 issues
+//    every TMA load from one thread.  The two tiles ping-pong: the tensor cores
+//    work on one tile's products while the other tile's softmax runs.
+//  * Base-2 exponentials with log2(e) folded into the scale (deep dive,
+//    "Implementation notes").  The running max is updated lazily: only when a row's
+//    max grows by more than 2^8 in the base-2 domain are l and the TMEM accumulator
+//    rescaled.  Exact: l and acc always refer to the same stale max, and the final
+//    O = acc / l and L = m + log2(l) use it too.
+//  * Every wait is time-limited; see ptx.cuh.
+#include <cfloat>
+#include <climits>
+#include <type_traits>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 320;          // 10 warps
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <typename T, int D>
+struct FwdCfg {
+    static constexpr bool kTF32 = std::is_same<T, float>::value;
+    static constexpr int kEB = static_cast<int>(sizeof(T));
+    static constexpr int kRowBytes = D * kEB;
+    static constexpr int kBoxCols = kBoxBytes / kEB;        // elements per 128-byte box row
+    static constexpr int kBoxes = kRowBytes / kBoxBytes;     // boxes per tile
+    static constexpr int kBoxTileBytes = kTileRows * kBoxBytes;
+    static constexpr int kTileBytes = kBoxes * kBoxTileBytes;
+    static constexpr int kKStep = 32 / kEB;                  // K elements per MMA instruction
+    static constexpr int kQKSteps = kRowBytes / 32;
+    static constexpr int kPVSteps = kTileRows / kKStep;
+    static constexpr int kStagesFit = (200 * 1024 - 2 * kTileBytes) / kTileBytes;
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    // shared memory map, offsets from a 1024-byte aligned base
+    static constexpr int kQOff = 0;
+    static constexpr int kKVOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+    static constexpr int kNumBars = 8 + 2 * kStages;
+    static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    // tensor memory columns
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kOCol = 256;
+    static constexpr uint32_t kFmt = kTF32 ? kFormatTF32 : kFormatBF16;
+    static constexpr uint32_t kIdescQK = make_idesc(kFmt, 128, 128, false, false);
+    static constexpr uint32_t kIdescPV = make_idesc(kFmt, 128, D, false, true);
+
+    static_assert(kRowBytes % kBoxBytes == 0, "row must be whole 128-byte boxes");
+    static_assert(kStages >= 2, "need at least two K/V stages");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(256 + 2 * D <= 512, "tensor memory budget");
+};
+
+// barrier indices
+template <int S> struct Bars {
+    static constexpr int kQ = 0;
+    static constexpr int kKVFull = 1;            // + stage
+    static constexpr int kKVEmpty = 1 + S;       // + stage
+    static constexpr int kSFull = 1 + 2 * S;     // + tile
+    static constexpr int kPFull = 3 + 2 * S;     // + tile
+    static constexpr int kODone = 5 + 2 * S;     // + tile
+    static constexpr int kMmaDone = 7 + 2 * S;
+};
+
+// wait-site ids recorded in the device status word
+enum : int {
+    kSiteLoadEmpty = 11, kSiteMmaQ = 12, kSiteMmaKV = 13, kSiteMmaP = 14, kSiteSoftS = 15,
+    kSiteSoftO = 16, kSiteEpiO = 17, kSiteDrain = 18, kSiteMmaDrain = 19
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+           const __grid_constant__ CUtensorMap tm_v, T *__restrict__ out, float *__restrict__ lse,
+           int N, int num_pairs, float scale_log2, int causal, unsigned int *status) {
+    using C = FwdCfg<T, D>;
+    using B = Bars<C::kStages>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    const uint32_t sQ = base + C::kQOff;
+    const uint32_t sKV = base + C::kKVOff;
+    const uint32_t sBar = base + C::kBarOff;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
+    const WaitCtx wc{abort_flag, status};
+    auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / num_pairs;
+    const int rank = blockIdx.x % num_pairs;
+    // heaviest pair first within a head when causal
+    const int pair = causal ? (num_pairs - 1 - rank) : rank;
+    const int nkv = (N + kTileRows - 1) / kTileRows;
+    int ntile[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int qt = 2 * pair + t;
+        ntile[t] = (qt * kTileRows >= N) ? 0 : (causal ? min(qt + 1, nkv) : nkv);
+    }
+    const int nmax = max(ntile[0], ntile[1]);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B::kQ), 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar(B::kKVFull + s), 1);
+            mbar_init(bar(B::kKVEmpty + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(B::kSFull + t), 1);
+            mbar_init(bar(B::kPFull + t), 128);
+            mbar_init(bar(B::kODone + t), 1);
+        }
+        mbar_init(bar(B::kMmaDone), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kLoadWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            uint32_t qbytes = 0;
+            for (int t = 0; t < 2; ++t) qbytes += ntile[t] > 0 ? C::kTileBytes : 0;
+            mbar_arrive_expect_tx(bar(B::kQ), qbytes);
+            for (int t = 0; t < 2; ++t) {
+                if (ntile[t] == 0) continue;
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_load_3d(sQ + t * C::kTileBytes + b * C::kBoxTileBytes, &tm_q, bar(B::kQ),
+                                b * C::kBoxCols, (2 * pair + t) * kTileRows, bh);
+            }
+            int seq = 0;
+            for (; seq < 2 * nmax; ++seq) {
+                const int s = seq % C::kStages;
+                const int use = seq / C::kStages;
+                if (use > 0 && !mbar_wait(bar(B::kKVEmpty + s), (use - 1) & 1, wc, kSiteLoadEmpty)) break;
+                mbar_arrive_expect_tx(bar(B::kKVFull + s), C::kTileBytes);
+                const CUtensorMap *m = (seq & 1) ? &tm_v : &tm_k;
+                const int j = seq >> 1;
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_load_3d(sKV + s * C::kTileBytes + b * C::kBoxTileBytes, m, bar(B::kKVFull + s),
+                                b * C::kBoxCols, j * kTileRows, bh);
+            }
+            // Every copy issued above must land before this CTA may exit.
+            mbar_wait_drain(bar(B::kQ), 0, wc, kSiteDrain);
+            for (int s = 0; s < C::kStages && s < seq; ++s) {
+                const int last = s + ((seq - 1 - s) / C::kStages) * C::kStages;
+                mbar_wait_drain(bar(B::kKVFull + s), (last / C::kStages) & 1, wc, kSiteDrain);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t tS[2] = {tmem, tmem + 128u};
+            const uint32_t tO[2] = {tmem + C::kOCol, tmem + C::kOCol + D};
+            auto wait_kv = [&](int seq) -> int {
+                const int s = seq % C::kStages;
+                if (!mbar_wait(bar(B::kKVFull + s), (seq / C::kStages) & 1, wc, kSiteMmaKV)) return -1;
+                tc_fence_after();
+                return s;
+            };
+            auto issue_qk = [&](int t, int s) {
+#pragma unroll
+                for (int kk = 0; kk < C::kQKSteps; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32;
+                    const uint64_t a = sdesc_sw128(sQ + t * C::kTileBytes + off, 16, 1024);
+                    const uint64_t b = sdesc_sw128(sKV + s * C::kTileBytes + off, 16, 1024);
+                    mma_ss<C::kTF32>(tS[t], a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int s, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::kPVSteps; ++kk) {
+                    const uint64_t b = sdesc_sw128(sKV + s * C::kTileBytes + kk * C::kKStep * kBoxBytes,
+                                                   C::kBoxTileBytes, 1024);
+                    mma_ts<C::kTF32>(tO[t], tS[t] + kk * 8u, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = mbar_wait(bar(B::kQ), 0, wc, kSiteMmaQ);
+            if (ok) {
+                const int sk = wait_kv(0);
+                ok = sk >= 0;
+                if (ok) {
+                    for (int t = 0; t < 2; ++t) {
+                        if (ntile[t] == 0) continue;
+                        issue_qk(t, sk);
+                        mma_commit(bar(B::kSFull + t));
+                    }
+                    mma_commit(bar(B::kKVEmpty + sk));
+                }
+            }
+            for (int j = 0; ok && j < nmax; ++j) {
+                const int sv = wait_kv(2 * j + 1);
+                if (sv < 0) { ok = false; break; }
+                int skn = -1;
+                for (int t = 0; t < 2; ++t) {
+                    if (j >= ntile[t]) continue;
+                    if (!mbar_wait(bar(B::kPFull + t), j & 1, wc, kSiteMmaP)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(t, sv, j > 0);
+                    mma_commit(bar(B::kODone + t));
+                    if (j + 1 < ntile[t]) {
+                        if (skn < 0) {
+                            skn = wait_kv(2 * (j + 1));
+                            if (skn < 0) { ok = false; break; }
+                        }
+                        issue_qk(t, skn);
+                        mma_commit(bar(B::kSFull + t));
+                    }
+                }
+                if (!ok) break;
+                mma_commit(bar(B::kKVEmpty + sv));
+                if (skn >= 0) mma_commit(bar(B::kKVEmpty + skn));
+            }
+            // Drain the tensor pipe before tensor memory can be released.
+            mma_commit(bar(B::kMmaDone));
+            mbar_wait_drain(bar(B::kMmaDone), 0, wc, kSiteMmaDrain);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = warp >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int row_g = (2 * pair + t) * kTileRows + row;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tSr = tmem + lane_off + 128u * t;
+        const uint32_t tOr = tmem + lane_off + C::kOCol + D * t;
+        float m_run = -INFINITY;  // running max, base-2 scaled units
+        float l_run = 0.f;        // running sum of 2^(s*scale_log2 - m_run)
+        bool ok = true;
+        for (int j = 0; j < ntile[t]; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kSFull + t), j & 1, wc, kSiteSoftS));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[128];
+            tmem_ld_x128(tSr, sr);
+            // mask: causal (key > query) and keys past N in the last tile
+            const int kv0 = j * kTileRows;
+            const int lim = min(causal ? row_g - kv0 : kTileRows - 1, N - 1 - kv0);
+            if (lim < kTileRows - 1) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+                mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+                mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+                mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
+                mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+            }
+            const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
+            float alpha = 1.f;
+            const bool upd = mx > m_run + kRescaleThreshold;
+            if (upd) {
+                alpha = ex2(m_run - mx);
+                m_run = mx;
+            }
+            const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
+            float sum0 = 0.f, sum1 = 0.f;
+            if constexpr (C::kTF32) {
+#pragma unroll
+                for (int c = 0; c < 128; c += 2) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sr[c]), scale_log2, neg));
+                    const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), scale_log2, neg));
+                    sum0 += p0;
+                    sum1 += p1;
+                    sr[c] = __float_as_uint(p0);
+                    sr[c + 1] = __float_as_uint(p1);
+                }
+                tmem_st_x128(tSr, sr);
+            } else {
+                uint32_t pk[64];
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), scale_log2, neg));
+                    const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, neg));
+                    sum0 += p0;
+                    sum1 += p1;
+                    pk[c] = pack_bf16(p0, p1);
+                }
+                tmem_st_x64(tSr, pk);
+            }
+            l_run = l_run * alpha + (sum0 + sum1);
+            if (j > 0 && __any_sync(0xffffffffu, upd)) {
+                // O still holds sum_{j' < j} P V relative to the old max: rescale it once
+                // the previous P V product has landed.
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kODone + t), (j - 1) & 1, wc, kSiteSoftO));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tOr + 32u * c, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st_x32(tOr + 32u * c, o);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(B::kPFull + t));
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok && ntile[t] > 0) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(bar(B::kODone + t), (ntile[t] - 1) & 1, wc, kSiteEpiO));
+            if (ok) {
+                tc_fence_after();
+                const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+                const bool valid = row_g < N;
+                T *orow = out + (static_cast<int64_t>(bh) * N + (valid ? row_g : 0)) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tOr + 32u * c, o);
+                    if (valid) {
+                        if constexpr (C::kTF32) {
+                            float4 *dst = reinterpret_cast<float4 *>(orow + 32 * c);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l,
+                                                     __uint_as_float(o[4 * i + 1]) * inv_l,
+                                                     __uint_as_float(o[4 * i + 2]) * inv_l,
+                                                     __uint_as_float(o[4 * i + 3]) * inv_l);
+                        } else {
+                            uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                uint4 w;
+                                w.x = pack_bf16(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l);
+                                w.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l);
+                                w.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l);
+                                w.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l);
+                                dst[i] = w;
+                            }
+                        }
+                    }
+                }
+                if (valid)
+                    lse[static_cast<int64_t>(bh) * N + row_g] =
+                        l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_fwd_t(const FwdArgs &a, cudaStream_t stream) {
+    using C = FwdCfg<T, D>;
+    auto kern = fwd_kernel<T, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int num_pairs = (a.N + 2 * kTileRows - 1) / (2 * kTileRows);
+    const long long blocks = static_cast<long long>(a.BH) * num_pairs;
+    if (blocks <= 0 || blocks > INT_MAX) return cudaErrorInvalidValue;
+    const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+    kern<<<static_cast<unsigned>(blocks), kThreads, C::kSmemBytes, stream>>>(
+        a.tm_q, a.tm_k, a.tm_v, static_cast<T *>(a.o), a.lse, a.N, num_pairs, scale_log2, a.causal,
+        a.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const FwdArgs &a, cudaStream_t stream) {
+    if (a.d == 64) return launch_fwd_t<__nv_bfloat16, 64>(a, stream);
+    if (a.d == 128) return launch_fwd_t<__nv_bfloat16, 128>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t stream) {
+    if (a.d == 64) return launch_fwd_t<float, 64>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

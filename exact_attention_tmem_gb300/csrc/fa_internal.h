@@ -1,0 +1,47 @@
+// fa_internal.h — host-side declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Per-launch description of one [BH, N, d] problem, filled by the ABI layer after
+// argument checks.  Tensor maps view a [BH, N, d] tensor as 3-D (d innermost, then
+// N, then BH) so that rows past N read as zeros and are never written.
+struct FwdArgs {
+    CUtensorMap tm_q, tm_k, tm_v;
+    void *o;
+    float *lse;
+    int N, BH, d;
+    float scale;
+    int causal;
+    unsigned int *status;  // device status word
+};
+
+struct BwdArgs {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;
+    const void *o, *dout;
+    const float *lse;
+    void *dq, *dk, *dv;
+    float *dq_acc;      // workspace: [BH, N, d] fp32
+    float *delta;       // workspace: [BH, Npad] fp32, D = rowsum(dO o O)
+    float *lse2;        // workspace: [BH, Npad] fp32, logsumexp in base 2 (+inf on padding rows)
+    int N, Npad, BH, d;
+    float scale;
+    int causal;
+    unsigned int *status;
+};
+
+// Kernel launchers (fa_fwd.cu, fa_bwd.cu).  They return the launch's cudaError_t.
+cudaError_t launch_fwd_bf16(const FwdArgs &a, cudaStream_t stream);
+cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t stream);
+cudaError_t launch_bwd_bf16(const BwdArgs &a, cudaStream_t stream);
+
+// Tile geometry shared by host and device code.
+constexpr int kTileRows = 128;     // rows of Q, K, V per tile
+constexpr int kBoxBytes = 128;     // inner extent of one TMA box (the 128-byte swizzle span)
+
+}  // namespace fa

@@ -1,0 +1,130 @@
+/*
+ * fa.h — exact softmax attention on GB300 (sm_103a): the C ABI.
+ *
+ * The library computes O = softmax(scale * Q K^T) V tile by tile with an online
+ * softmax, so the N x N score matrix never reaches device memory, and stores one
+ * logsumexp per query row; the backward pass recomputes the probabilities from
+ * that logsumexp.  Sources, by page and section:
+ *   - "FlashAttention" (deep dive, tirogla.com), section "How it works": inputs
+ *     Q, K, V of shape N x d per head, outputs O and one logsumexp per row, no
+ *     state between calls; L = m + log l; the backward pass recomputes
+ *     P = exp(Q K^T * scale - L) and uses D = rowsum(dO o O), dS = P o (dP - D).
+ *   - "tm_flash_attention_arch_2k", section "End-to-end forward pass": the
+ *     [B, H, N, d] layout; section "The architecture: every step explained":
+ *     causal blocks above the diagonal have no effect and are skipped.
+ *   - "FlashAttention" (deep dive), section "Code" (the GPU kernel): tensors
+ *     contiguous as (B*H, N, d), 64-bit offsets; section "Pitfalls": int32
+ *     offset overflow, fully masked rows.
+ *
+ * Conventions shared by every entry point:
+ *   - Layout: q, k, v, o, dO, dq, dk, dv are [B, H, N, d] contiguous (row stride
+ *     d elements, head stride N*d); lse is [B, H, N] float32.  Queries and keys
+ *     have the same length N.
+ *   - Masking: causal != 0 applies the square, top-left aligned mask: key j is
+ *     visible to query i iff j <= i.  causal == 0 attends to all N keys.
+ *   - lse holds the natural-log logsumexp of the scaled scores over the visible
+ *     keys: lse_i = log(sum_j exp(scale * q_i . k_j)).
+ *   - Pointers are device pointers (the _host entry points excepted), 16-byte
+ *     aligned (the tensor-memory-access engine needs it); lse 4-byte aligned.
+ *   - Ownership: the caller allocates and owns every buffer, workspaces
+ *     included.  The library allocates no device memory, keeps no state
+ *     between calls (beyond per-device one-time set-up) and never synchronises
+ *     the stream: work is enqueued on `stream` and the call returns.  Inputs
+ *     are read only; outputs are fully overwritten.
+ *   - Errors: every entry point returns an fa_status.  Argument errors are
+ *     detected on the host before anything is enqueued.  A device-side wait
+ *     that exceeds its time limit sets a device status word, read with
+ *     fa_get_device_status().  No C++ exception and no exit() crosses this ABI.
+ *   - Supported: head dim d in {64, 128}; N >= 1 of any value; B*H*N*d below
+ *     2^62; compute capability 10.3 (GB300).
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,     /* NULL pointer, B/H/N < 1, non-finite scale, size overflow */
+    FA_ERR_UNSUPPORTED = 2,     /* d not supported, or the device is not compute capability 10.3 */
+    FA_ERR_ALIGNMENT = 3,       /* a pointer is not 16-byte aligned (lse: 4-byte) */
+    FA_ERR_WORKSPACE = 4,       /* workspace NULL or smaller than fa_bwd_workspace_size() */
+    FA_ERR_CUDA = 5,            /* a CUDA runtime/driver call failed; see fa_last_cuda_error() */
+    FA_ERR_DEVICE_TIMEOUT = 6   /* a device-side wait gave up (read via fa_get_device_status) */
+} fa_status;
+
+/*
+ * Forward pass, bf16 storage, fp32 accumulation.
+ *   q, k, v  [B,H,N,d] bf16, read only
+ *   o        [B,H,N,d] bf16, written: softmax(scale * q k^T [masked]) v
+ *   lse      [B,H,N]   fp32, written: natural-log logsumexp per query row
+ *   scale    multiplies the raw dot products (usually 1/sqrt(d)); must be finite
+ * Page: "FlashAttention" (deep dive), section "How it works" (the forward loop
+ * with running max m, running sum l and accumulator acc; O = acc / l and
+ * L = m + log l are the only outputs).
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
+
+/*
+ * Forward pass with float32 inputs and outputs (same layout and meaning as
+ * fa_fwd; q, k, v, o are float32).  The two products run on the tensor cores
+ * in TF32 with fp32 accumulation.  Supported for d = 64 only.
+ */
+int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,
+               int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for a problem of this size: the fp32
+ * dQ accumulator plus two fp32 per-row vectors (D = rowsum(dO o O) and the
+ * logsumexp in base 2), padded to whole 128-row tiles.  Returns 0 if the
+ * arguments are invalid.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass, bf16 storage, fp32 accumulation.
+ *   q, k, v, o  [B,H,N,d] bf16, read only (o and lse as written by fa_fwd)
+ *   lse         [B,H,N]   fp32, read only
+ *   dout        [B,H,N,d] bf16, read only: gradient of the loss w.r.t. o
+ *   dq, dk, dv  [B,H,N,d] bf16, written: gradients w.r.t. q, k, v
+ *   workspace   device buffer of at least fa_bwd_workspace_size(B,H,N,d)
+ *               bytes, 256-byte aligned; its contents on entry do not matter
+ *               and are scratch on exit
+ * The dQ contributions of different key blocks are summed with fp32 atomic
+ * adds, so dq can differ from run to run in the last bits.
+ * Page: "FlashAttention" (deep dive), section "How it works" (backward
+ * recomputes P = exp(Q K^T * scale - L), D = rowsum(dO o O),
+ * dS = P o (dP - D)); the scale enters dQ and dK by the chain rule.
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv, void *workspace,
+           size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+           fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT if a kernel gave up
+ * waiting since the last call (its outputs are then undefined).  Returns
+ * FA_ERR_CUDA if the synchronisation itself failed.
+ */
+int fa_get_device_status(fa_stream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *fa_status_string(int status);
+
+/* The cudaError_t of the last call that returned FA_ERR_CUDA in this thread. */
+int fa_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,153 @@
+"""The C-ABI library: it loads, exports every declared entry point, and rejects bad
+arguments on the host with the documented status codes (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_tmem_gb300 import _lib
+from exact_attention_tmem_gb300 import buildlib as build_mod
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fa.h")
+
+A = 0x10000   # fake, 16-byte aligned "device" addresses: never dereferenced on the host
+W = 0x20000
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(_lib.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_status_strings(lib):
+    for code in range(0, 7):
+        s = _lib.status_string(code)
+        assert s and s != "unknown status"
+    assert _lib.status_string(99) == "unknown status"
+
+
+def fwd(lib, q=A, k=A, v=A, o=A, lse=A, B=1, H=1, N=128, d=128, scale=0.1, causal=0, f32=False):
+    fn = lib.fa_fwd_f32 if f32 else lib.fa_fwd
+    return fn(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), causal, None)
+
+
+def bwd(lib, ptrs=None, ws=W, ws_bytes=None, B=1, H=1, N=128, d=128, scale=0.1):
+    p = [A] * 9 if ptrs is None else ptrs
+    if ws_bytes is None:
+        ws_bytes = lib.fa_bwd_workspace_size(B, H, N, d) if B > 0 and H > 0 and N > 0 else 0
+    return lib.fa_bwd(*p, ws, ws_bytes, B, H, N, d, ctypes.c_float(scale), 1, None)
+
+
+@pytest.mark.parametrize("which", range(5))
+def test_fwd_null_pointer(lib, which):
+    ptrs = [A] * 5
+    ptrs[which] = None
+    assert fwd(lib, *ptrs) == _lib.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("B,H,N", [(0, 1, 8), (1, 0, 8), (1, 1, 0), (-1, 1, 8), (1, 1, -5)])
+def test_fwd_bad_sizes(lib, B, H, N):
+    assert fwd(lib, B=B, H=H, N=N) == _lib.FA_ERR_INVALID_ARG
+
+
+def test_fwd_size_overflow(lib):
+    # B*H above INT_MAX, and B*H*N*d above 2^62
+    assert fwd(lib, B=1 << 20, H=1 << 20, N=8) == _lib.FA_ERR_INVALID_ARG
+    assert fwd(lib, B=1 << 15, H=1 << 15, N=(1 << 31) - 1) == _lib.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("scale", [float("nan"), float("inf"), float("-inf")])
+def test_fwd_non_finite_scale(lib, scale):
+    assert fwd(lib, scale=scale) == _lib.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d", [1, 32, 96, 256])
+def test_fwd_unsupported_head_dim(lib, d):
+    assert fwd(lib, d=d) == _lib.FA_ERR_UNSUPPORTED
+
+
+def test_fwd_f32_only_d64(lib):
+    assert fwd(lib, d=128, f32=True) == _lib.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("which,addr", [(0, A + 8), (1, A + 2), (2, A + 4), (3, A + 1), (4, A + 2)])
+def test_fwd_misaligned(lib, which, addr):
+    ptrs = [A] * 5
+    ptrs[which] = addr
+    assert fwd(lib, *ptrs) == _lib.FA_ERR_ALIGNMENT
+
+
+def test_fwd_lse_needs_only_4_byte_alignment(lib):
+    # lse at A+4 passes the host checks; what follows needs a device
+    st = fwd(lib, lse=A + 4)
+    assert st in (_lib.FA_ERR_CUDA, _lib.FA_ERR_UNSUPPORTED) or st == _lib.FA_OK
+
+
+def test_workspace_size(lib):
+    B, H, N, d = 2, 3, 300, 64
+    npad = 384
+    acc = B * H * N * d * 4
+    vec = -(-(B * H * npad * 4) // 256) * 256
+    assert lib.fa_bwd_workspace_size(B, H, N, d) == -(-acc // 256) * 256 + 2 * vec
+    assert lib.fa_bwd_workspace_size(0, 1, 8, 64) == 0
+    assert lib.fa_bwd_workspace_size(1, 1, 8, 96) == 0
+
+
+@pytest.mark.parametrize("which", range(9))
+def test_bwd_null_pointer(lib, which):
+    ptrs = [A] * 9
+    ptrs[which] = None
+    assert bwd(lib, ptrs) == _lib.FA_ERR_INVALID_ARG
+
+
+def test_bwd_workspace_checks(lib):
+    assert bwd(lib, ws=None) == _lib.FA_ERR_WORKSPACE
+    need = lib.fa_bwd_workspace_size(1, 1, 128, 128)
+    assert bwd(lib, ws_bytes=need - 1) == _lib.FA_ERR_WORKSPACE
+    assert bwd(lib, ws=W + 16) == _lib.FA_ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("which", [0, 1, 2, 3, 5, 6, 7, 8])
+def test_bwd_misaligned(lib, which):
+    ptrs = [A] * 9
+    ptrs[which] = A + 8
+    assert bwd(lib, ptrs) == _lib.FA_ERR_ALIGNMENT
+
+
+def test_bwd_bad_shape(lib):
+    assert bwd(lib, B=0) == _lib.FA_ERR_INVALID_ARG
+    assert bwd(lib, d=96, ws_bytes=1 << 30) == _lib.FA_ERR_UNSUPPORTED
+    assert bwd(lib, scale=float("nan")) == _lib.FA_ERR_INVALID_ARG
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert fwd(lib) == _lib.FA_ERR_CUDA
+    assert _lib.last_cuda_error() != 0
+    assert lib.fa_get_device_status(None) == _lib.FA_ERR_CUDA
+
+
+def test_python_binding_raises_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        _lib.load()
