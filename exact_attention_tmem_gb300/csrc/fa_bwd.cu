@@ -1,6 +1,597 @@
-// fa_bwd.cu — backward pass (in progress).
+// fa_bwd.cu — backward pass of exact attention on sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes ("FlashAttention" deep dive, section "How it works": the backward
+// pass recomputes P = exp(Q K^T * scale - L) per tile from the saved L, then uses
+// D = rowsum(dO o O) and dS = P o (dP - D) to form dQ, dK and dV).  With the scale
+// inside S, the chain rule gives dV = P^T dO, dP = dO V^T, dK = scale * dS^T Q and
+// dQ = scale * dS K.
+//
+// Three kernels on the caller's stream:
+//  1. bwd_pre:  D_i = sum_t dO_it O_it (fp32), the logsumexp in base 2 (L * log2 e),
+//               both padded to whole 128-row tiles (padding rows get D = 0 and
+//               L = +inf, so their probabilities are exactly 0), and the fp32 dQ
+//               accumulator cleared.
+//  2. bwd_main: one CTA per (batch*head, 128-key block j).  K_j and V_j stay in
+//               shared memory; the CTA walks the query blocks i (i >= j when causal:
+//               blocks above the diagonal are skipped) and per block runs five
+//               tcgen05 products:
+//                 S^T  = K_j Q_i^T          (TMEM)        -> P^T = 2^(S^T*scale*log2e - L2_i)
+//                 dP^T = V_j dO_i^T         (TMEM)        -> dS^T = P^T o (dP^T - D_i)
+//                 dV  += P^T dO_i           (A = P^T from TMEM)
+//                 dK  += dS^T Q_i           (A = dS^T from TMEM)
+//                 dQ_i = dS K_j             (A = dS from shared memory) -> fp32 atomics
+//               dK and dV accumulate in TMEM for the whole walk and are written once.
+//  3. bwd_post: dQ = bf16(scale * accumulator).
+//
+// Tensor memory (512 columns): dK [0, d) | dV [d, 2d) | S^T [2d, 2d+128) | dP^T [2d+128,
+// 2d+256).  P^T (bf16) is written over the first 64 S^T columns, dS^T over the first 64
+// dP^T columns, and dQ_i accumulates in the dP^T columns once dK has consumed dS^T.
+//
+// Warp roles (320 threads): warps 0-3 own one key row each (softmax recompute and dS),
+// warps 4-7 own one query row each (dQ read-out and atomics), warp 8 issues the MMAs,
+// warp 9 issues the TMA loads.  Every wait is time-limited (see ptx.cuh).
+#include <climits>
+
 #include "fa_internal.h"
+#include "ptx.cuh"
 
 namespace fa {
-cudaError_t launch_bwd_bf16(const BwdArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kBoxes = D * 2 / kBoxBytes;
+    static constexpr int kBoxTileBytes = kTileRows * kBoxBytes;    // 16 KB
+    static constexpr int kTileBytes = kBoxes * kBoxTileBytes;
+    static constexpr int kQStages = 2;
+    static constexpr int kDOStages = (D == 128) ? 1 : 2;
+    static constexpr int kVecBytes = kTileRows * 4;                 // 128 fp32
+    static constexpr int kDSBytes = 2 * kBoxTileBytes;              // 128 x 128 bf16
+    // shared memory map (offsets from a 1024-byte aligned base)
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kKOff + kTileBytes;
+    static constexpr int kQOff = kVOff + kTileBytes;
+    static constexpr int kDOOff = kQOff + kQStages * kTileBytes;
+    static constexpr int kDSOff = kDOOff + kDOStages * kTileBytes;
+    // the base-2 logsumexp and D of query block i travel with Q_i (one stage)
+    static constexpr int kLOff = kDSOff + kDSBytes;
+    static constexpr int kDOff = kLOff + kQStages * kVecBytes;
+    static constexpr int kBarOff = kDOff + kQStages * kVecBytes;
+    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 7;
+    static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    // tensor memory
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kDKCol = 0;
+    static constexpr uint32_t kDVCol = D;
+    static constexpr uint32_t kSCol = 2 * D;
+    static constexpr uint32_t kDPCol = 2 * D + 128;
+    static constexpr int kKSteps = D / 16;          // K steps over the head dim
+    static constexpr int kRowSteps = kTileRows / 16; // K steps over 128 rows
+    static constexpr uint32_t kIdescSS = make_idesc(kFormatBF16, 128, 128, false, false);
+    static constexpr uint32_t kIdescTS = make_idesc(kFormatBF16, 128, D, false, true);
+    static constexpr uint32_t kIdescDQ = make_idesc(kFormatBF16, 128, D, true, true);
+
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(2 * D + 256 <= 512, "tensor memory budget");
+};
+
+template <int QS, int DS>
+struct BwdBars {
+    static constexpr int kKV = 0;
+    static constexpr int kQFull = 1;                 // + stage
+    static constexpr int kQEmpty = 1 + QS;           // + stage
+    static constexpr int kDOFull = 1 + 2 * QS;       // + stage
+    static constexpr int kDOEmpty = 1 + 2 * QS + DS; // + stage
+    static constexpr int kSFull = 1 + 2 * QS + 2 * DS;
+    static constexpr int kDPFull = kSFull + 1;
+    static constexpr int kPFull = kSFull + 2;
+    static constexpr int kDSFull = kSFull + 3;
+    static constexpr int kDQFull = kSFull + 4;
+    static constexpr int kDQFree = kSFull + 5;
+    static constexpr int kDrain = kSFull + 6;
+};
+
+enum : int {
+    kSiteBLoadQ = 31, kSiteBLoadDO = 32, kSiteBMmaKV = 33, kSiteBMmaQ = 34, kSiteBMmaDO = 35,
+    kSiteBMmaP = 36, kSiteBMmaDS = 37, kSiteBMmaDQ = 38, kSiteBSoftS = 39, kSiteBSoftL = 40,
+    kSiteBSoftDP = 41, kSiteBDQ = 43, kSiteBEpi = 44, kSiteBDrain = 45
+};
+
+// ------------------------------------------------------------------------------------
+// 1. pre-processing: D, base-2 logsumexp (padded), cleared dQ accumulator
+// ------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256)
+bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
+               const float *__restrict__ lse, float *__restrict__ delta, float *__restrict__ lse2,
+               float *__restrict__ dq_acc, int N, int Npad, int BH) {
+    constexpr int kLanesPerRow = D / 8;              // 16-byte chunks per row
+    constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / kLanesPerRow;
+    const int part = lane % kLanesPerRow;
+    const long long warp_global = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    const long long total_rows = static_cast<long long>(BH) * Npad;
+    for (long long base = warp_global * kRowsPerWarp; base < total_rows; base += nwarps * kRowsPerWarp) {
+        const long long r = base + sub;
+        float acc = 0.f;
+        bool valid = false;
+        long long src_row = 0;
+        if (r < total_rows) {
+            const long long bh = r / Npad;
+            const int i = static_cast<int>(r % Npad);
+            valid = i < N;
+            src_row = bh * N + i;
+            if (valid) {
+                const uint4 a = reinterpret_cast<const uint4 *>(o + src_row * D)[part];
+                const uint4 b = reinterpret_cast<const uint4 *>(dout + src_row * D)[part];
+                const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
+                const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float2 fa = __bfloat1622float2(pa[t]);
+                    const float2 fb = __bfloat1622float2(pb[t]);
+                    acc = fmaf(fa.x, fb.x, acc);
+                    acc = fmaf(fa.y, fb.y, acc);
+                }
+            }
+        }
+#pragma unroll
+        for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (r < total_rows && part == 0) {
+            delta[r] = valid ? acc : 0.f;
+            lse2[r] = valid ? lse[src_row] * kLog2e : INFINITY;
+        }
+    }
+    const long long n4 = static_cast<long long>(BH) * N * D / 4;
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+    float4 *acc4 = reinterpret_cast<float4 *>(dq_acc);
+    for (long long x = tid; x < n4; x += nthreads) acc4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------------------------
+// 3. post-processing: dQ = bf16(scale * accumulator)
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+bwd_post_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq, long long n8, float scale) {
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+    const float4 *src = reinterpret_cast<const float4 *>(dq_acc);
+    uint4 *dst = reinterpret_cast<uint4 *>(dq);
+    for (long long x = tid; x < n8; x += nthreads) {
+        const float4 a = src[2 * x], b = src[2 * x + 1];
+        uint4 w;
+        w.x = pack_bf16(a.x * scale, a.y * scale);
+        w.y = pack_bf16(a.z * scale, a.w * scale);
+        w.z = pack_bf16(b.x * scale, b.y * scale);
+        w.w = pack_bf16(b.z * scale, b.w * scale);
+        dst[x] = w;
+    }
+}
+
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// ------------------------------------------------------------------------------------
+// 2. main kernel
+// ------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const float *__restrict__ lse2, const float *__restrict__ delta, float *__restrict__ dq_acc,
+                __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int N, int Npad, int nkv,
+                float scale, float scale_log2, int causal, unsigned int *status) {
+    using C = BwdCfg<D>;
+    using B = BwdBars<C::kQStages, C::kDOStages>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    const uint32_t sK = base + C::kKOff, sV = base + C::kVOff, sQ = base + C::kQOff;
+    const uint32_t sDO = base + C::kDOOff, sDS = base + C::kDSOff;
+    const uint32_t sL = base + C::kLOff, sD = base + C::kDOff, sBar = base + C::kBarOff;
+    const float *Lvec = reinterpret_cast<const float *>(smem + C::kLOff);
+    const float *Dvec = reinterpret_cast<const float *>(smem + C::kDOff);
+    uint8_t *dS_ptr = smem + C::kDSOff;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
+    const WaitCtx wc{abort_flag, status};
+    auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / nkv;
+    const int j = blockIdx.x % nkv;          // key block; j = 0 (the longest walk) first
+    const int nq = Npad / kTileRows;
+    const int i0 = causal ? j : 0;
+    const int n_it = nq - i0;                // >= 1
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B::kKV), 1);
+        for (int s = 0; s < C::kQStages; ++s) {
+            mbar_init(bar(B::kQFull + s), 1);
+            mbar_init(bar(B::kQEmpty + s), 1);
+        }
+        for (int s = 0; s < C::kDOStages; ++s) {
+            mbar_init(bar(B::kDOFull + s), 1);
+            mbar_init(bar(B::kDOEmpty + s), 1);
+        }
+        mbar_init(bar(B::kSFull), 1);
+        mbar_init(bar(B::kDPFull), 1);
+        mbar_init(bar(B::kPFull), 128);
+        mbar_init(bar(B::kDSFull), 128);
+        mbar_init(bar(B::kDQFull), 1);
+        mbar_init(bar(B::kDQFree), 128);
+        mbar_init(bar(B::kDrain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kLoadWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_do);
+            mbar_arrive_expect_tx(bar(B::kKV), 2 * C::kTileBytes);
+            for (int b = 0; b < C::kBoxes; ++b) {
+                tma_load_3d(sK + b * C::kBoxTileBytes, &tm_k, bar(B::kKV), b * 64, j * kTileRows, bh);
+                tma_load_3d(sV + b * C::kBoxTileBytes, &tm_v, bar(B::kKV), b * 64, j * kTileRows, bh);
+            }
+            const float *lrow = lse2 + static_cast<int64_t>(bh) * Npad;
+            const float *drow = delta + static_cast<int64_t>(bh) * Npad;
+            int q_loads = 0, do_loads = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int i = i0 + it;
+                const int qs = it % C::kQStages, qu = it / C::kQStages;
+                if (qu > 0 && !mbar_wait(bar(B::kQEmpty + qs), (qu - 1) & 1, wc, kSiteBLoadQ)) break;
+                mbar_arrive_expect_tx(bar(B::kQFull + qs), C::kTileBytes + 2 * C::kVecBytes);
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_load_3d(sQ + qs * C::kTileBytes + b * C::kBoxTileBytes, &tm_q, bar(B::kQFull + qs),
+                                b * 64, i * kTileRows, bh);
+                bulk_load(sL + qs * C::kVecBytes, lrow + i * kTileRows, C::kVecBytes, bar(B::kQFull + qs));
+                bulk_load(sD + qs * C::kVecBytes, drow + i * kTileRows, C::kVecBytes, bar(B::kQFull + qs));
+                ++q_loads;
+                const int ds = it % C::kDOStages, du = it / C::kDOStages;
+                if (du > 0 && !mbar_wait(bar(B::kDOEmpty + ds), (du - 1) & 1, wc, kSiteBLoadDO)) break;
+                mbar_arrive_expect_tx(bar(B::kDOFull + ds), C::kTileBytes);
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_load_3d(sDO + ds * C::kTileBytes + b * C::kBoxTileBytes, &tm_do, bar(B::kDOFull + ds),
+                                b * 64, i * kTileRows, bh);
+                ++do_loads;
+            }
+            // Every copy issued above must land before this CTA may exit: wait for the
+            // last fill of every stage.
+            mbar_wait_drain(bar(B::kKV), 0, wc, kSiteBDrain);
+            for (int s = 0; s < C::kQStages && s < q_loads; ++s) {
+                const int last = s + ((q_loads - 1 - s) / C::kQStages) * C::kQStages;
+                mbar_wait_drain(bar(B::kQFull + s), (last / C::kQStages) & 1, wc, kSiteBDrain);
+            }
+            for (int s = 0; s < C::kDOStages && s < do_loads; ++s) {
+                const int last = s + ((do_loads - 1 - s) / C::kDOStages) * C::kDOStages;
+                mbar_wait_drain(bar(B::kDOFull + s), (last / C::kDOStages) & 1, wc, kSiteBDrain);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t tDK = tmem + C::kDKCol, tDV = tmem + C::kDVCol;
+            const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDPCol;
+            auto wait_q = [&](int it) -> int {
+                const int s = it % C::kQStages;
+                if (!mbar_wait(bar(B::kQFull + s), (it / C::kQStages) & 1, wc, kSiteBMmaQ)) return -1;
+                tc_fence_after();
+                return s;
+            };
+            auto wait_do = [&](int it) -> int {
+                const int s = it % C::kDOStages;
+                if (!mbar_wait(bar(B::kDOFull + s), (it / C::kDOStages) & 1, wc, kSiteBMmaDO)) return -1;
+                tc_fence_after();
+                return s;
+            };
+            // K-major x K-major product over the head dim: D[128 x 128] = A B^T
+            auto mma_kk = [&](uint32_t d_tmem, uint32_t a_s, uint32_t b_s) {
+#pragma unroll
+                for (int kk = 0; kk < C::kKSteps; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32;
+                    mma_ss<false>(d_tmem, sdesc_sw128(a_s + off, 16, 1024), sdesc_sw128(b_s + off, 16, 1024),
+                                  C::kIdescSS, kk > 0 ? 1u : 0u);
+                }
+            };
+            // A from TMEM (128 x 128, bf16 packed), B MN-major [128 rows x D]
+            auto mma_tn = [&](uint32_t d_tmem, uint32_t a_tmem, uint32_t b_s, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < C::kRowSteps; ++kk)
+                    mma_ts<false>(d_tmem, a_tmem + kk * 8u,
+                                  sdesc_sw128(b_s + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024), C::kIdescTS,
+                                  (acc || kk > 0) ? 1u : 0u);
+            };
+            bool ok = mbar_wait(bar(B::kKV), 0, wc, kSiteBMmaKV);
+            tc_fence_after();
+            int qs = -1, dos = -1;
+            if (ok) {
+                qs = wait_q(0);
+                ok = qs >= 0;
+            }
+            if (ok) {
+                mma_kk(tS, sK, sQ + qs * C::kTileBytes);
+                mma_commit(bar(B::kSFull));
+                dos = wait_do(0);
+                ok = dos >= 0;
+            }
+            if (ok) {
+                mma_kk(tDP, sV, sDO + dos * C::kTileBytes);
+                mma_commit(bar(B::kDPFull));
+            }
+            for (int it = 0; ok && it < n_it; ++it) {
+                // dV += P^T dO_i
+                if (!mbar_wait(bar(B::kPFull), it & 1, wc, kSiteBMmaP)) { ok = false; break; }
+                tc_fence_after();
+                mma_tn(tDV, tS, sDO + dos * C::kTileBytes, it > 0);
+                mma_commit(bar(B::kDOEmpty + dos));
+                // S^T for the next query block
+                int qs_next = -1;
+                if (it + 1 < n_it) {
+                    qs_next = wait_q(it + 1);
+                    if (qs_next < 0) { ok = false; break; }
+                    mma_kk(tS, sK, sQ + qs_next * C::kTileBytes);
+                    mma_commit(bar(B::kSFull));
+                }
+                // dK += dS^T Q_i ;  dQ_i = dS K_j
+                if (!mbar_wait(bar(B::kDSFull), it & 1, wc, kSiteBMmaDS)) { ok = false; break; }
+                tc_fence_after();
+                mma_tn(tDK, tDP, sQ + qs * C::kTileBytes, it > 0);
+                mma_commit(bar(B::kQEmpty + qs));
+#pragma unroll
+                for (int kk = 0; kk < C::kRowSteps; ++kk)
+                    mma_ss<false>(tDP, sdesc_sw128(sDS + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024),
+                                  sdesc_sw128(sK + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024), C::kIdescDQ,
+                                  kk > 0 ? 1u : 0u);
+                mma_commit(bar(B::kDQFull));
+                qs = qs_next;
+                // dP^T for the next query block, once dQ_i has been read out of its columns
+                if (it + 1 < n_it) {
+                    if (!mbar_wait(bar(B::kDQFree), it & 1, wc, kSiteBMmaDQ)) { ok = false; break; }
+                    tc_fence_after();
+                    dos = wait_do(it + 1);
+                    if (dos < 0) { ok = false; break; }
+                    mma_kk(tDP, sV, sDO + dos * C::kTileBytes);
+                    mma_commit(bar(B::kDPFull));
+                }
+            }
+            // Drain the tensor pipe before tensor memory can be released.
+            mma_commit(bar(B::kDrain));
+            mbar_wait_drain(bar(B::kDrain), 0, wc, kSiteBDrain);
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ key rows: P^T and dS^T
+        const int c = warp * 32 + lane;                     // key row within the block
+        const int kg = j * kTileRows + c;                   // global key index
+        const bool key_valid = kg < N;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tSr = tmem + lane_off + C::kSCol;
+        const uint32_t tDPr = tmem + lane_off + C::kDPCol;
+        // this thread's row of dS^T in the MN-major, 128-byte swizzled shared tile
+        uint8_t *ds_row0 = dS_ptr + c * kBoxBytes;
+        const int swz = c & 7;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int i = i0 + it;
+            const int qs = it % C::kQStages;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kSFull), it & 1, wc, kSiteBSoftS) &&
+                                             mbar_wait(bar(B::kQFull + qs), (it / C::kQStages) & 1, wc, kSiteBSoftL));
+            if (!ok) break;
+            tc_fence_after();
+            float p[128];
+            {
+                uint32_t sr[128];
+                tmem_ld_x128(tSr, sr);
+                const float *L = Lvec + qs * kTileRows;
+                // causal: query q sees key c iff c <= q (same block offsets on the diagonal)
+                const int qmin = (causal && i == j) ? c : 0;
+#pragma unroll
+                for (int q = 0; q < 128; ++q) {
+                    const float e = ex2(fmaf(__uint_as_float(sr[q]), scale_log2, -L[q]));
+                    p[q] = (key_valid && q >= qmin) ? e : 0.f;
+                }
+            }
+            {
+                uint32_t pk[64];
+#pragma unroll
+                for (int q = 0; q < 64; ++q) pk[q] = pack_bf16(p[2 * q], p[2 * q + 1]);
+                tmem_st_x64(tSr, pk);
+            }
+            tc_fence_before();
+            mbar_arrive(bar(B::kPFull));
+            // dS^T = P^T o (dP^T - D)
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDPFull), it & 1, wc, kSiteBSoftDP));
+            if (!ok) break;
+            tc_fence_after();
+            const float *Dv = Dvec + qs * kTileRows;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {                 // 32 query columns at a time
+                uint32_t r[32];
+                tmem_ld_x32(tDPr + 32u * ch, r);
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const int q0 = 32 * ch + 2 * t;
+                    const float d0 = p[q0] * (__uint_as_float(r[2 * t]) - Dv[q0]);
+                    const float d1 = p[q0 + 1] * (__uint_as_float(r[2 * t + 1]) - Dv[q0 + 1]);
+                    pk[t] = pack_bf16(d0, d1);
+                }
+                // shared: query columns 32*ch .. 32*ch+31 = box (ch / 2), 16-byte chunks
+                // 4*(ch % 2) .. 4*(ch % 2)+3 of this key's row
+                uint8_t *box = ds_row0 + (ch >> 1) * C::kBoxTileBytes;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int chunk = 4 * (ch & 1) + u;
+                    *reinterpret_cast<uint4 *>(box + ((chunk ^ swz) << 4)) =
+                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                }
+                // tensor memory: dS^T packed over the first 64 dP^T columns
+                uint32_t (&half)[16] = pk;
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                    "%12, %13, %14, %15, %16};\n\t" ::"r"(tDPr + 16u * ch),
+                    "r"(half[0]), "r"(half[1]), "r"(half[2]), "r"(half[3]), "r"(half[4]), "r"(half[5]),
+                    "r"(half[6]), "r"(half[7]), "r"(half[8]), "r"(half[9]), "r"(half[10]), "r"(half[11]),
+                    "r"(half[12]), "r"(half[13]), "r"(half[14]), "r"(half[15])
+                    : "memory");
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B::kDSFull));
+        }
+        // ------------------------------------------------------------ epilogue: dV row
+        if (ok) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDQFull), (n_it - 1) & 1, wc, kSiteBEpi));
+        }
+        if (ok) {
+            tc_fence_after();
+            __nv_bfloat16 *row = dv + (static_cast<int64_t>(bh) * N + (key_valid ? kg : 0)) * D;
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld_x32(tmem + lane_off + C::kDVCol + 32u * ch, r);
+                if (key_valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(row + 32 * ch);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        dst[u] = make_uint4(pack_bf16(__uint_as_float(r[8 * u]), __uint_as_float(r[8 * u + 1])),
+                                            pack_bf16(__uint_as_float(r[8 * u + 2]), __uint_as_float(r[8 * u + 3])),
+                                            pack_bf16(__uint_as_float(r[8 * u + 4]), __uint_as_float(r[8 * u + 5])),
+                                            pack_bf16(__uint_as_float(r[8 * u + 6]), __uint_as_float(r[8 * u + 7])));
+                }
+            }
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ query rows: dQ read-out
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;                   // query row within the block
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tDQr = tmem + lane_off + C::kDPCol;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int i = i0 + it;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDQFull), it & 1, wc, kSiteBDQ));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t v[D / 32][32];
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) tmem_ld_x32(tDQr + 32u * ch, v[ch]);
+            tc_fence_before();
+            mbar_arrive(bar(B::kDQFree));
+            const int qg = i * kTileRows + r;
+            if (qg < N) {
+                float *dst = dq_acc + (static_cast<int64_t>(bh) * N + qg) * D;
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch)
+#pragma unroll
+                    for (int t = 0; t < 32; t += 4)
+                        red_add_v4(dst + 32 * ch + t, __uint_as_float(v[ch][t]), __uint_as_float(v[ch][t + 1]),
+                                   __uint_as_float(v[ch][t + 2]), __uint_as_float(v[ch][t + 3]));
+            }
+        }
+        // ------------------------------------------------------------ epilogue: dK row
+        if (ok) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDQFull), (n_it - 1) & 1, wc, kSiteBEpi));
+        }
+        if (ok) {
+            tc_fence_after();
+            const int kg = j * kTileRows + r;
+            const bool key_valid = kg < N;
+            __nv_bfloat16 *row = dk + (static_cast<int64_t>(bh) * N + (key_valid ? kg : 0)) * D;
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t v[32];
+                tmem_ld_x32(tmem + lane_off + C::kDKCol + 32u * ch, v);
+                if (key_valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(row + 32 * ch);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        dst[u] = make_uint4(
+                            pack_bf16(__uint_as_float(v[8 * u]) * scale, __uint_as_float(v[8 * u + 1]) * scale),
+                            pack_bf16(__uint_as_float(v[8 * u + 2]) * scale, __uint_as_float(v[8 * u + 3]) * scale),
+                            pack_bf16(__uint_as_float(v[8 * u + 4]) * scale, __uint_as_float(v[8 * u + 5]) * scale),
+                            pack_bf16(__uint_as_float(v[8 * u + 6]) * scale, __uint_as_float(v[8 * u + 7]) * scale));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+int grid_for(long long work_items, int per_block) {
+    long long g = (work_items + per_block - 1) / per_block;
+    if (g < 1) g = 1;
+    if (g > 152LL * 16) g = 152LL * 16;
+    return static_cast<int>(g);
+}
+
+template <int D>
+cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
+    using C = BwdCfg<D>;
+    const long long rows = static_cast<long long>(a.BH) * a.Npad;
+    bwd_pre_kernel<D><<<grid_for(rows, 64), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(a.o), static_cast<const __nv_bfloat16 *>(a.dout), a.lse, a.delta,
+        a.lse2, a.dq_acc, a.N, a.Npad, a.BH);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    auto kern = bwd_main_kernel<D>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int nkv = a.Npad / kTileRows;
+    const long long blocks = static_cast<long long>(a.BH) * nkv;
+    if (blocks <= 0 || blocks > INT_MAX) return cudaErrorInvalidValue;
+    const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+    kern<<<static_cast<unsigned>(blocks), kThreads, C::kSmemBytes, stream>>>(
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, a.dq_acc, static_cast<__nv_bfloat16 *>(a.dk),
+        static_cast<__nv_bfloat16 *>(a.dv), a.N, a.Npad, nkv, a.scale, scale_log2, a.causal, a.status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    const long long n8 = static_cast<long long>(a.BH) * a.N * D / 8;
+    bwd_post_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(a.dq_acc, static_cast<__nv_bfloat16 *>(a.dq), n8,
+                                                           a.scale);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_bf16(const BwdArgs &a, cudaStream_t stream) {
+    if (a.d == 64) return launch_bwd_t<64>(a, stream);
+    if (a.d == 128) return launch_bwd_t<128>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace fa

@@ -81,7 +81,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // and records `site` in the device status word).
 // With `honour_abort` false the wait ignores the abort flag (used to drain copies
 // still in flight before a CTA exits), but it is still time-limited.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtx ctx, int site,
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtx ctx, int site,
                                             bool honour_abort) {
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {

@@ -3,7 +3,9 @@ seeded inputs, run the fp64 oracle on the same (rounded) values, compare.
 
 Tolerances (bf16 storage, fp32 accumulation), from the workload specification:
 max |dO| <= 2e-2 on O, max |dL| <= 5e-3 on the logsumexp, and for each gradient
-tensor max |error| <= 5e-2 * max |oracle gradient|.
+tensor max |error| <= 5e-2 * max |oracle gradient| + 1e-4.  The absolute 1e-4 term
+only matters where the exact gradient vanishes identically (N = 1: dQ = dK = 0),
+where the relative bound alone would reject fp32 rounding noise (~1e-7).
 """
 from __future__ import annotations
 
@@ -18,6 +20,7 @@ from exact_attention_tmem_gb300 import inputs
 TOL_O = 2e-2
 TOL_L = 5e-3
 TOL_GRAD_REL = 5e-2
+TOL_GRAD_ABS = 1e-4
 
 
 def to_dev(*ts):
@@ -57,6 +60,6 @@ def assert_fwd_close(o, lse, o_ref, lse_ref, what=""):
 def assert_grad_close(g, g_ref, name, what=""):
     scale = float(np.max(np.abs(g_ref))) if g_ref.size else 0.0
     e = max_err(g, g_ref)
-    assert e <= TOL_GRAD_REL * max(scale, 1e-30), \
-        f"{what}: {name} max error {e:.3e} > {TOL_GRAD_REL} * {scale:.3e}"
+    assert e <= TOL_GRAD_REL * scale + TOL_GRAD_ABS, \
+        f"{what}: {name} max error {e:.3e} > {TOL_GRAD_REL} * {scale:.3e} + {TOL_GRAD_ABS}"
     return e / max(scale, 1e-30)
