@@ -207,6 +207,7 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
     const size_t acc_aligned = (acc + 255) / 256 * 256;
     const size_t vec = (static_cast<size_t>(BH) * npad * sizeof(float) + 255) / 256 * 256;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if ((st = make_tmap(&a.tm_dq, ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH)) != FA_OK) return st;
     a.o = o;
     a.dout = dout;
     a.lse = lse;

@@ -19,8 +19,10 @@
 //                 dP^T = V_j dO_i^T         (TMEM)        -> dS^T = P^T o (dP^T - D_i)
 //                 dV  += P^T dO_i           (A = P^T from TMEM)
 //                 dK  += dS^T Q_i           (A = dS^T from TMEM)
-//                 dQ_i = dS K_j             (A = dS from shared memory) -> fp32 atomics
-//               dK and dV accumulate in TMEM for the whole walk and are written once.
+//                 dQ_i = dS K_j             (A = dS from shared memory)
+//               dQ_i leaves tensor memory through a 32 KB shared staging tile and
+//               TMA bulk reduce-add (fp32) into the dQ accumulator; dK and dV
+//               accumulate in TMEM for the whole walk and are written once.
 //  3. bwd_post: dQ = bf16(scale * accumulator).
 //
 // Tensor memory (512 columns): dK [0, d) | dV [d, 2d) | S^T [2d, 2d+128) | dP^T [2d+128,
@@ -28,8 +30,11 @@
 // dP^T columns, and dQ_i accumulates in the dP^T columns once dK has consumed dS^T.
 //
 // Warp roles (320 threads): warps 0-3 own one key row each (softmax recompute and dS),
-// warps 4-7 own one query row each (dQ read-out and atomics), warp 8 issues the MMAs,
-// warp 9 issues the TMA loads.  Every wait is time-limited (see ptx.cuh).
+// warps 4-7 own one query row each (dQ read-out, staging and bulk reduce), warp 8
+// issues the MMAs, warp 9 issues the TMA loads.  Every wait is time-limited (see
+// ptx.cuh).  The shared-memory budget at d = 128 is within 1 KB of the 227 KB limit,
+// so the kernel relies on the dynamic shared window starting 1024-byte aligned and
+// checks it instead of over-allocating (a misaligned start is reported, not used).
 #include <climits>
 
 #include "fa_internal.h"
@@ -52,6 +57,9 @@ struct BwdCfg {
     static constexpr int kDOStages = (D == 128) ? 1 : 2;
     static constexpr int kVecBytes = kTileRows * 4;                 // 128 fp32
     static constexpr int kDSBytes = 2 * kBoxTileBytes;              // 128 x 128 bf16
+    static constexpr int kDQHalfCols = 64;                          // fp32 columns per staging pass
+    static constexpr int kDQPasses = D / kDQHalfCols;
+    static constexpr int kDQStageBytes = kTileRows * kDQHalfCols * 4; // 32 KB = 2 boxes of 32 fp32
     // shared memory map (offsets from a 1024-byte aligned base)
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kKOff + kTileBytes;
@@ -59,12 +67,13 @@ struct BwdCfg {
     static constexpr int kDOOff = kQOff + kQStages * kTileBytes;
     static constexpr int kDSOff = kDOOff + kDOStages * kTileBytes;
     // the base-2 logsumexp and D of query block i travel with Q_i (one stage)
-    static constexpr int kLOff = kDSOff + kDSBytes;
+    static constexpr int kDQOff = kDSOff + kDSBytes;
+    static constexpr int kLOff = kDQOff + kDQStageBytes;
     static constexpr int kDOff = kLOff + kQStages * kVecBytes;
     static constexpr int kBarOff = kDOff + kQStages * kVecBytes;
     static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 7;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
-    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    static constexpr int kSmemBytes = kMiscOff + 16;
     // tensor memory
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kDKCol = 0;
@@ -100,7 +109,7 @@ struct BwdBars {
 enum : int {
     kSiteBLoadQ = 31, kSiteBLoadDO = 32, kSiteBMmaKV = 33, kSiteBMmaQ = 34, kSiteBMmaDO = 35,
     kSiteBMmaP = 36, kSiteBMmaDS = 37, kSiteBMmaDQ = 38, kSiteBSoftS = 39, kSiteBSoftL = 40,
-    kSiteBSoftDP = 41, kSiteBDQ = 43, kSiteBEpi = 44, kSiteBDrain = 45
+    kSiteBSoftDP = 41, kSiteBMisaligned = 42, kSiteBDQ = 43, kSiteBEpi = 44, kSiteBDrain = 45
 };
 
 // ------------------------------------------------------------------------------------
@@ -177,11 +186,6 @@ bwd_post_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq
     }
 }
 
-__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-
 // ------------------------------------------------------------------------------------
 // 2. main kernel
 // ------------------------------------------------------------------------------------
@@ -189,21 +193,26 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const float *__restrict__ lse2, const float *__restrict__ delta, float *__restrict__ dq_acc,
+                const __grid_constant__ CUtensorMap tm_dq, const float *__restrict__ lse2,
+                const float *__restrict__ delta,
                 __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int N, int Npad, int nkv,
                 float scale, float scale_log2, int causal, unsigned int *status) {
     using C = BwdCfg<D>;
     using B = BwdBars<C::kQStages, C::kDOStages>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *smem = smem_raw + (base - raw);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = smem_u32(smem_raw);
+    if ((base & 1023u) != 0) {  // see the note at the top of this file
+        if (threadIdx.x == 0 && atomicOr(&status[0], kStatusTimeout) == 0u) status[1] = kSiteBMisaligned;
+        return;
+    }
+    uint8_t *smem = smem_raw;
     const uint32_t sK = base + C::kKOff, sV = base + C::kVOff, sQ = base + C::kQOff;
-    const uint32_t sDO = base + C::kDOOff, sDS = base + C::kDSOff;
+    const uint32_t sDO = base + C::kDOOff, sDS = base + C::kDSOff, sDQ = base + C::kDQOff;
     const uint32_t sL = base + C::kLOff, sD = base + C::kDOff, sBar = base + C::kBarOff;
     const float *Lvec = reinterpret_cast<const float *>(smem + C::kLOff);
     const float *Dvec = reinterpret_cast<const float *>(smem + C::kDOff);
     uint8_t *dS_ptr = smem + C::kDSOff;
+    uint8_t *dQ_stage = smem + C::kDQOff;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
     const WaitCtx wc{abort_flag, status};
@@ -253,6 +262,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_do);
+            tma_prefetch_desc(&tm_dq);
             mbar_arrive_expect_tx(bar(B::kKV), 2 * C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b) {
                 tma_load_3d(sK + b * C::kBoxTileBytes, &tm_k, bar(B::kKV), b * 64, j * kTileRows, bh);
@@ -402,7 +412,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                              mbar_wait(bar(B::kQFull + qs), (it / C::kQStages) & 1, wc, kSiteBSoftL));
             if (!ok) break;
             tc_fence_after();
-            float p[128];
+            // P^T = 2^(S^T * scale*log2e - L2) in fp32, kept as packed bf16: the same values
+            // feed the dV product (from TMEM) and dS below.
+            uint32_t pk[64];
             {
                 uint32_t sr[128];
                 tmem_ld_x128(tSr, sr);
@@ -410,17 +422,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // causal: query q sees key c iff c <= q (same block offsets on the diagonal)
                 const int qmin = (causal && i == j) ? c : 0;
 #pragma unroll
-                for (int q = 0; q < 128; ++q) {
-                    const float e = ex2(fmaf(__uint_as_float(sr[q]), scale_log2, -L[q]));
-                    p[q] = (key_valid && q >= qmin) ? e : 0.f;
+                for (int q = 0; q < 128; q += 2) {
+                    const float e0 = ex2(fmaf(__uint_as_float(sr[q]), scale_log2, -L[q]));
+                    const float e1 = ex2(fmaf(__uint_as_float(sr[q + 1]), scale_log2, -L[q + 1]));
+                    pk[q >> 1] = pack_bf16((key_valid && q >= qmin) ? e0 : 0.f,
+                                           (key_valid && q + 1 >= qmin) ? e1 : 0.f);
                 }
             }
-            {
-                uint32_t pk[64];
-#pragma unroll
-                for (int q = 0; q < 64; ++q) pk[q] = pack_bf16(p[2 * q], p[2 * q + 1]);
-                tmem_st_x64(tSr, pk);
-            }
+            tmem_st_x64(tSr, pk);
             tc_fence_before();
             mbar_arrive(bar(B::kPFull));
             // dS^T = P^T o (dP^T - D)
@@ -432,13 +441,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int ch = 0; ch < 4; ++ch) {                 // 32 query columns at a time
                 uint32_t r[32];
                 tmem_ld_x32(tDPr + 32u * ch, r);
-                uint32_t pk[16];
+                uint32_t dk2[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     const int q0 = 32 * ch + 2 * t;
-                    const float d0 = p[q0] * (__uint_as_float(r[2 * t]) - Dv[q0]);
-                    const float d1 = p[q0 + 1] * (__uint_as_float(r[2 * t + 1]) - Dv[q0 + 1]);
-                    pk[t] = pack_bf16(d0, d1);
+                    const uint32_t pp = pk[16 * ch + t];
+                    const float p0 = __uint_as_float(pp << 16), p1 = __uint_as_float(pp & 0xffff0000u);
+                    dk2[t] = pack_bf16(p0 * (__uint_as_float(r[2 * t]) - Dv[q0]),
+                                       p1 * (__uint_as_float(r[2 * t + 1]) - Dv[q0 + 1]));
                 }
                 // shared: query columns 32*ch .. 32*ch+31 = box (ch / 2), 16-byte chunks
                 // 4*(ch % 2) .. 4*(ch % 2)+3 of this key's row
@@ -447,16 +457,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int u = 0; u < 4; ++u) {
                     const int chunk = 4 * (ch & 1) + u;
                     *reinterpret_cast<uint4 *>(box + ((chunk ^ swz) << 4)) =
-                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                        make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
                 }
-                // tensor memory: dS^T packed over the first 64 dP^T columns
-                uint32_t (&half)[16] = pk;
+                // tensor memory: dS^T packed over the first 64 dP^T columns (these columns
+                // have already been read: chunk ch reads 32ch.., writes 16ch..)
                 asm volatile(
                     "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
                     "%12, %13, %14, %15, %16};\n\t" ::"r"(tDPr + 16u * ch),
-                    "r"(half[0]), "r"(half[1]), "r"(half[2]), "r"(half[3]), "r"(half[4]), "r"(half[5]),
-                    "r"(half[6]), "r"(half[7]), "r"(half[8]), "r"(half[9]), "r"(half[10]), "r"(half[11]),
-                    "r"(half[12]), "r"(half[13]), "r"(half[14]), "r"(half[15])
+                    "r"(dk2[0]), "r"(dk2[1]), "r"(dk2[2]), "r"(dk2[3]), "r"(dk2[4]), "r"(dk2[5]),
+                    "r"(dk2[6]), "r"(dk2[7]), "r"(dk2[8]), "r"(dk2[9]), "r"(dk2[10]), "r"(dk2[11]),
+                    "r"(dk2[12]), "r"(dk2[13]), "r"(dk2[14]), "r"(dk2[15])
                     : "memory");
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -495,7 +505,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int i = i0 + it;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDQFull), it & 1, wc, kSiteBDQ));
+            // all 128 threads leave together, so none is left waiting at a named barrier
+            ok = named_barrier_and(1, 128, mbar_wait(bar(B::kDQFull), it & 1, wc, kSiteBDQ));
             if (!ok) break;
             tc_fence_after();
             uint32_t v[D / 32][32];
@@ -503,17 +514,35 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int ch = 0; ch < D / 32; ++ch) tmem_ld_x32(tDQr + 32u * ch, v[ch]);
             tc_fence_before();
             mbar_arrive(bar(B::kDQFree));
-            const int qg = i * kTileRows + r;
-            if (qg < N) {
-                float *dst = dq_acc + (static_cast<int64_t>(bh) * N + qg) * D;
+            // Stage 64 fp32 columns at a time as two 128-byte-swizzled boxes of 32 columns
+            // (row r = 128 bytes per box) and add them into the accumulator with one TMA
+            // bulk reduction per box.  Rows past N fall outside the tensor map and are
+            // dropped by the reduction.
 #pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch)
+            for (int pass = 0; pass < C::kDQPasses; ++pass) {
 #pragma unroll
-                    for (int t = 0; t < 32; t += 4)
-                        red_add_v4(dst + 32 * ch + t, __uint_as_float(v[ch][t]), __uint_as_float(v[ch][t + 1]),
-                                   __uint_as_float(v[ch][t + 2]), __uint_as_float(v[ch][t + 3]));
+                for (int b = 0; b < 2; ++b) {
+                    uint8_t *row = dQ_stage + b * C::kBoxTileBytes + r * kBoxBytes;
+                    const uint32_t(&src)[32] = v[2 * pass + b];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        *reinterpret_cast<uint4 *>(row + ((u ^ (r & 7)) << 4)) =
+                            make_uint4(src[4 * u], src[4 * u + 1], src[4 * u + 2], src[4 * u + 3]);
+                }
+                fence_proxy_async_smem();
+                named_barrier_sync(1, 128);
+                if (threadIdx.x == 128) {
+#pragma unroll
+                    for (int b = 0; b < 2; ++b)
+                        tma_reduce_add_3d(&tm_dq, sDQ + b * C::kBoxTileBytes, pass * C::kDQHalfCols + 32 * b,
+                                          i * kTileRows, bh);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();
+                }
+                named_barrier_sync(1, 128);
             }
         }
+        if (threadIdx.x == 128) bulk_wait_group0();
         // ------------------------------------------------------------ epilogue: dK row
         if (ok) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDQFull), (n_it - 1) & 1, wc, kSiteBEpi));
@@ -575,7 +604,7 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
     if (blocks <= 0 || blocks > INT_MAX) return cudaErrorInvalidValue;
     const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     kern<<<static_cast<unsigned>(blocks), kThreads, C::kSmemBytes, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, a.dq_acc, static_cast<__nv_bfloat16 *>(a.dk),
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.lse2, a.delta, static_cast<__nv_bfloat16 *>(a.dk),
         static_cast<__nv_bfloat16 *>(a.dv), a.N, a.Npad, nkv, a.scale, scale_log2, a.causal, a.status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -23,6 +23,7 @@ struct FwdArgs {
 
 struct BwdArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;
+    CUtensorMap tm_dq;  // the fp32 dQ accumulator, boxes of 32 columns x 128 rows
     const void *o, *dout;
     const float *lse;
     void *dq, *dk, *dv;

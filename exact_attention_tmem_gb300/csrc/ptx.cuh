@@ -136,6 +136,42 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// 3-D tiled bulk reduction shared -> global: the box at (x, y, z) is added (fp32 add)
+// element-wise into global memory; elements outside the tensor are skipped.  Completion
+// is tracked with bulk async-groups (bulk_commit_group / bulk_wait_group*).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until the shared-memory sources of every committed bulk group have been read.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until every committed bulk group has completed (global writes performed).
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Barrier over `count` threads (a multiple of 32) with hardware barrier `id` (1..15).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Barrier over `count` threads that also returns the AND of `pred` over them: used to
+// make a give-up decision uniform before a group enters further named barriers.
+__device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %3, 0;\n\t"
+        "bar.red.and.pred p, %1, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(out)
+        : "r"(id), "r"(count), "r"(pred ? 1u : 0u)
+        : "memory");
+    return out != 0;
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy
 // reads (tcgen05.mma operands written with st.shared).
 __device__ __forceinline__ void fence_proxy_async_smem() {
