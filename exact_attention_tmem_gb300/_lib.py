@@ -22,8 +22,9 @@ FA_ERR_WORKSPACE = 4
 FA_ERR_CUDA = 5
 FA_ERR_DEVICE_TIMEOUT = 6
 
-EXPORTED = ("fa_fwd", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_get_device_status",
-            "fa_status_string", "fa_last_cuda_error")
+EXPORTED = ("fa_fwd", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_noalloc",
+            "fa_get_device_status", "fa_status_string", "fa_last_cuda_error")
+NOALLOC_SCRATCH_BYTES = 64 << 20   # FA_NOALLOC_SCRATCH_BYTES in include/fa.h
 
 _lock = threading.Lock()
 _lib = None
@@ -55,6 +56,8 @@ def load() -> ctypes.CDLL:
         lib.fa_bwd_workspace_size.restype = Z
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, Z, I, I, I, I, F, I, vp]
         lib.fa_bwd.restype = I
+        lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, vp]
+        lib.fa_bwd_noalloc.restype = I
         lib.fa_get_device_status.argtypes = [vp]
         lib.fa_get_device_status.restype = I
         lib.fa_status_string.argtypes = [I]

@@ -109,6 +109,29 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
            fa_stream_t stream);
 
+/* Size in bytes of the scratch array built into the library for fa_bwd_noalloc. */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * Backward pass without a workspace argument, for callers that cannot allocate device
+ * memory (a plugin handed only tensors by a framework that owns all device memory, a
+ * loop that must not call cudaMalloc, a process with a fixed memory budget).  The pages
+ * have no counterpart: this is a convenience of this library.
+ *   Arguments, layouts and results are those of fa_bwd; the workspace is a device
+ *   array of FA_NOALLOC_SCRATCH_BYTES inside the library (held by every GPU that loads
+ *   the library until the process exits).
+ *   Returns FA_ERR_WORKSPACE when fa_bwd_workspace_size(B, H, N, d) exceeds
+ *   FA_NOALLOC_SCRATCH_BYTES (use fa_bwd with a caller-owned workspace instead);
+ *   otherwise the same statuses as fa_bwd.
+ *   The first call on a device looks up the array's device address (with that device
+ *   current); make that first call before any stream capture.  All calls share the
+ *   array, so calls whose kernels overlap on the GPU (e.g. on two streams) race.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                   const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                   float scale, int causal, fa_stream_t stream);
+
 /*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT if a kernel gave up
