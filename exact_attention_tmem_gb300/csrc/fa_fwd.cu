@@ -55,12 +55,18 @@ struct FwdCfg {
     static constexpr int kQKSteps = kRowBytes / 32;
     static constexpr int kPVSteps = kTileRows / kKStep;
     static constexpr int kStagesFit = (200 * 1024 - 2 * kTileBytes) / kTileBytes;
-    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    // TF32: two stages, so K always lands in stage 0 and V in stage 1 (see kVtOff)
+    static constexpr int kStages = kTF32 ? 2 : (kStagesFit > 8 ? 8 : kStagesFit);
     // shared memory map, offsets from a 1024-byte aligned base
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kTileBytes;
-    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
-    static constexpr int kNumBars = 8 + 2 * kStages;
+    // TF32 only: V^T of the current V tile, K-major (the TF32 B operand must be K-major):
+    // 4 boxes of 32 keys (128 bytes) x D rows.
+    static constexpr int kVtOff = kKVOff + kStages * kTileBytes;
+    static constexpr int kVtBoxBytes = D * kBoxBytes;
+    static constexpr int kVtBytes = kTF32 ? 4 * kVtBoxBytes : 0;
+    static constexpr int kBarOff = kVtOff + kVtBytes;
+    static constexpr int kNumBars = 9 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     // tensor memory columns
@@ -68,7 +74,7 @@ struct FwdCfg {
     static constexpr uint32_t kOCol = 256;
     static constexpr uint32_t kFmt = kTF32 ? kFormatTF32 : kFormatBF16;
     static constexpr uint32_t kIdescQK = make_idesc(kFmt, 128, 128, false, false);
-    static constexpr uint32_t kIdescPV = make_idesc(kFmt, 128, D, false, true);
+    static constexpr uint32_t kIdescPV = make_idesc(kFmt, 128, D, false, !kTF32);
 
     static_assert(kRowBytes % kBoxBytes == 0, "row must be whole 128-byte boxes");
     static_assert(kStages >= 2, "need at least two K/V stages");
@@ -85,6 +91,7 @@ template <int S> struct Bars {
     static constexpr int kPFull = 3 + 2 * S;     // + tile
     static constexpr int kODone = 5 + 2 * S;     // + tile
     static constexpr int kMmaDone = 7 + 2 * S;
+    static constexpr int kVtFull = 8 + 2 * S;    // TF32: V^T of the current V tile written
 };
 
 // wait-site ids recorded in the device status word
@@ -139,6 +146,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             mbar_init(bar(B::kODone + t), 1);
         }
         mbar_init(bar(B::kMmaDone), 1);
+        mbar_init(bar(B::kVtFull), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -151,7 +159,70 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kLoadWarp) {
+    if (warp == kLoadWarp && C::kTF32) {
+        // ------------------------------------------------------------ TMA producer, TF32
+        // As below, and the whole warp transposes each landed V tile into V^T (K-major),
+        // then signals kVtFull.  V tiles are every second fill, always stage 1.
+        const uint32_t sVt = base + C::kVtOff;
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            uint32_t qbytes = 0;
+            for (int t = 0; t < 2; ++t) qbytes += ntile[t] > 0 ? C::kTileBytes : 0;
+            mbar_arrive_expect_tx(bar(B::kQ), qbytes);
+            for (int t = 0; t < 2; ++t) {
+                if (ntile[t] == 0) continue;
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_load_3d(sQ + t * C::kTileBytes + b * C::kBoxTileBytes, &tm_q, bar(B::kQ),
+                                b * C::kBoxCols, (2 * pair + t) * kTileRows, bh);
+            }
+        }
+        int seq = 0;
+        for (; seq < 2 * nmax; ++seq) {
+            const int s = seq % C::kStages;
+            const int use = seq / C::kStages;
+            bool ok = true;
+            if (lane == 0) {
+                if (use > 0) ok = mbar_wait(bar(B::kKVEmpty + s), (use - 1) & 1, wc, kSiteLoadEmpty);
+                if (ok) {
+                    mbar_arrive_expect_tx(bar(B::kKVFull + s), C::kTileBytes);
+                    const CUtensorMap *m = (seq & 1) ? &tm_v : &tm_k;
+                    for (int b = 0; b < C::kBoxes; ++b)
+                        tma_load_3d(sKV + s * C::kTileBytes + b * C::kBoxTileBytes, m, bar(B::kKVFull + s),
+                                    b * C::kBoxCols, (seq >> 1) * kTileRows, bh);
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (seq & 1) {
+                // V tile: wait for it, then write V^T.  Element (key k, column n) sits in box
+                // n / 32 at row k, 16-byte chunk ((n % 32) / 4) ^ (k % 8); in V^T it goes to
+                // box k / 32 at row n, chunk ((k % 32) / 4) ^ (n % 8).
+                if (!__all_sync(0xffffffffu, mbar_wait(bar(B::kKVFull + s), use & 1, wc, kSiteLoadEmpty))) break;
+                const uint8_t *vsrc = smem + C::kKVOff + s * C::kTileBytes;
+                uint8_t *vdst = smem + C::kVtOff;
+                for (int idx = lane; idx < kTileRows * D; idx += 32) {
+                    const int k = idx / D, n = idx % D;
+                    const int nb = n % 32, kb = k % 32;
+                    const float val = *reinterpret_cast<const float *>(
+                        vsrc + (n / 32) * C::kBoxTileBytes + k * kBoxBytes + ((((nb >> 2) ^ (k & 7)) << 4) | ((nb & 3) << 2)));
+                    *reinterpret_cast<float *>(vdst + (k / 32) * C::kVtBoxBytes + n * kBoxBytes +
+                                               ((((kb >> 2) ^ (n & 7)) << 4) | ((kb & 3) << 2))) = val;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B::kVtFull));
+            }
+        }
+        (void)sVt;
+        if (lane == 0) {
+            mbar_wait_drain(bar(B::kQ), 0, wc, kSiteDrain);
+            for (int s = 0; s < C::kStages && s < seq; ++s) {
+                const int last = s + ((seq - 1 - s) / C::kStages) * C::kStages;
+                mbar_wait_drain(bar(B::kKVFull + s), (last / C::kStages) & 1, wc, kSiteDrain);
+            }
+        }
+    } else if (warp == kLoadWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
@@ -208,8 +279,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             auto issue_pv = [&](int t, int s, bool acc) {
 #pragma unroll
                 for (int kk = 0; kk < C::kPVSteps; ++kk) {
-                    const uint64_t b = sdesc_sw128(sKV + s * C::kTileBytes + kk * C::kKStep * kBoxBytes,
-                                                   C::kBoxTileBytes, 1024);
+                    // bf16: V as an MN-major B operand; TF32: V^T as a K-major B operand
+                    const uint64_t b =
+                        C::kTF32 ? sdesc_sw128(base + C::kVtOff + (kk >> 2) * C::kVtBoxBytes + (kk & 3) * 32, 16, 1024)
+                                 : sdesc_sw128(sKV + s * C::kTileBytes + kk * C::kKStep * kBoxBytes,
+                                               C::kBoxTileBytes, 1024);
                     mma_ts<C::kTF32>(tO[t], tS[t] + kk * 8u, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
                 }
             };
@@ -227,7 +301,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 }
             }
             for (int j = 0; ok && j < nmax; ++j) {
-                const int sv = wait_kv(2 * j + 1);
+                int sv;
+                if constexpr (C::kTF32) {
+                    // V^T of V_j written by the producer warp (V tiles always use stage 1)
+                    sv = mbar_wait(bar(B::kVtFull), j & 1, wc, kSiteMmaKV) ? 1 : -1;
+                    tc_fence_after();
+                } else {
+                    sv = wait_kv(2 * j + 1);
+                }
                 if (sv < 0) { ok = false; break; }
                 int skn = -1;
                 for (int t = 0; t < 2; ++t) {
