@@ -165,9 +165,10 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_dict(w):
-    return {"workload": f"fwd+bwd causal bf16 B={w.B} H={w.H} N={w.N} d={w.d}",
-            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": CAUSAL, "scale": "1/sqrt(d)",
+def config_dict(w, shape=None):
+    B, H, N, d = shape if shape else (w.B, w.H, w.N, w.d)
+    return {"workload": f"fwd+bwd causal bf16 B={B} H={H} N={N} d={d}",
+            "B": B, "H": H, "N": N, "d": d, "causal": CAUSAL, "scale": "1/sqrt(d)",
             "inputs": "iid N(0,1) rounded to bf16, seeds 3001-3004",
             "l2": "inputs 512 MiB > L2; L2 flushed (256 MiB write) between timed steps",
             "parallelism": "one independent replica per GPU"}
@@ -182,9 +183,12 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     fa.build()
     w = inputs.WORKLOADS[WORKLOAD_ID]
-    B, H, N, d = w.B, w.H, w.N, w.d
+    B, H, N, d = args.shape if args.shape else (w.B, w.H, w.N, w.d)
     scale = 1.0 / math.sqrt(d)
-    q_h, k_h, v_h, do_h = inputs.workload_inputs(WORKLOAD_ID, with_grad_out=True)
+    if args.shape:
+        q_h, k_h, v_h, do_h = inputs.random_inputs(B, H, N, d, seed=WORKLOAD_ID, with_grad_out=True)
+    else:
+        q_h, k_h, v_h, do_h = inputs.workload_inputs(WORKLOAD_ID, with_grad_out=True)
     q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -204,7 +208,7 @@ def run_ours(args, world, rank, local):
     if fa.device_status() != 0:
         raise RuntimeError("device status reports a timed-out wait during warm-up")
 
-    fwd_flops = w.fwd_flops(CAUSAL)
+    fwd_flops = 4.0 * N * N * d * B * H / (2 if CAUSAL else 1)
     bwd_flops = 2.5 * fwd_flops
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if world > 1:
@@ -236,9 +240,53 @@ def run_ours(args, world, rank, local):
     bwd_tf = bwd_flops / (statistics.mean(t_bwd) * 1e-3) / 1e12
 
     # ---- end to end through the public API: pinned host inputs in, results back out
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, world, dev, stream, step, (q, k, v, do), (o, lse, dq, dk, dv),
+                      (q_h, k_h, v_h, do_h), fwd_flops + bwd_flops)
+    if rank != 0:
+        return
+    peak_burst, peak_sust, hbm, peak_src = peaks()
+    dominant = "bwd" if statistics.mean(t_bwd) >= statistics.mean(t_fwd) else "fwd"
+    dom_tf = bwd_tf if dominant == "bwd" else fwd_tf
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(w, args.shape),
+        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+        "fwd_ms": statistics.mean(t_fwd), "bwd_ms": statistics.mean(t_bwd),
+        "fwd_frac_of_peak": fwd_tf / peak_burst, "bwd_frac_of_peak": bwd_tf / peak_burst,
+        "roofline": {"bound": "tensor", "kernel": f"{dominant} (CUDA events around the C-ABI call)",
+                     "achieved": dom_tf, "peak": peak_burst, "unit": "TFLOP/s",
+                     "frac": dom_tf / peak_burst, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 burst"},
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "device_status": status,
+    }
+    clocks = clk.summary()
+    line["clocks"] = clocks
+    if world == 1 and not args.no_cpu_baseline:
+        rows = inputs.sample_rows(N, CPU_SAMPLE_ROWS, seed=7)
+        tf, dt, cores = cpu_oracle_sample(q_h, k_h, v_h, do_h, d, rows)
+        line["cpu_baseline"] = {
+            "value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": (f"{len(rows)} seeded query rows of each of the {B * H} heads, forward + "
+                       f"backward of those rows in fp64, {dt:.1f} s")}
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, world, dev, stream, step, dev_in, dev_out, host_in, flops):
+    """Same step through the public API with pinned host inputs copied in and every
+    output copied back, host-device copies inside the timed region."""
+    import torch
+    q, k, v, do = dev_in
+    o, lse, dq, dk, dv = dev_out
+    q_h, k_h, v_h, do_h = host_in
     hq, hk, hv, hdo = (t.pin_memory() for t in (q_h, k_h, v_h, do_h))
     ho, hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (q_h, q_h, k_h, v_h))
-    hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    hlse = torch.empty(tuple(lse.shape), dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
 
@@ -259,40 +307,8 @@ def run_ours(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    e2e_value = world * (fwd_flops + bwd_flops) / (e2e_ms * 1e-3) / 1e12
-
-    if rank != 0:
-        return
-    peak_burst, peak_sust, hbm, peak_src = peaks()
-    dominant = "bwd" if statistics.mean(t_bwd) >= statistics.mean(t_fwd) else "fwd"
-    dom_tf = bwd_tf if dominant == "bwd" else fwd_tf
-    line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(w),
-        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
-        "fwd_ms": statistics.mean(t_fwd), "bwd_ms": statistics.mean(t_bwd),
-        "fwd_frac_of_peak": fwd_tf / peak_burst, "bwd_frac_of_peak": bwd_tf / peak_burst,
-        "roofline": {"bound": "tensor", "kernel": f"{dominant} (CUDA events around the C-ABI call)",
-                     "achieved": dom_tf, "peak": peak_burst, "unit": "TFLOP/s",
-                     "frac": dom_tf / peak_burst, "traffic": None,
-                     "peak_source": f"{peak_src} bf16 burst"},
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 4 * args.steps,
-        "device_status": status,
-    }
-    clocks = clk.summary()
-    line["clocks"] = clocks
-    if world == 1 and not args.no_cpu_baseline:
-        rows = inputs.sample_rows(N, CPU_SAMPLE_ROWS, seed=7)
-        tf, dt, cores = cpu_oracle_sample(q_h, k_h, v_h, do_h, d, rows)
-        line["cpu_baseline"] = {
-            "value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": (f"{len(rows)} seeded query rows of each of the {B * H} heads, forward + "
-                       f"backward of those rows in fp64, {dt:.1f} s")}
-    print(json.dumps(line), flush=True)
+    return {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
 
 def main():
@@ -303,6 +319,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the fp64 oracle on the host")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--shape", type=lambda x: tuple(int(v) for v in x.split(",")), default=None,
+                    metavar="B,H,N,d",
+                    help="run another shape (profiling captures on a smaller case); the metric "
+                         "is defined on the default B=2,H=32,N=8192,d=128")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
