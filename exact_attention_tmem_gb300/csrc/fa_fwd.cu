@@ -360,13 +360,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 for (int c = 0; c < 128; ++c)
                     if (c > lim) sr[c] = __float_as_uint(-INFINITY);
             }
+            // row max: four independent chains of three-input max
             float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-                mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-                mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-                mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
-                mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+            for (int c = 0; c < 128; c += 8) {
+                mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                mx2 = max3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+                mx3 = max3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
             }
             const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
             float alpha = 1.f;
@@ -376,30 +377,33 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 m_run = mx;
             }
             const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
-            float sum0 = 0.f, sum1 = 0.f;
+            // P = 2^(s * scale_log2 - m): paired FFMA, two EX2, paired sums
+            const float2 sl2 = make_float2(scale_log2, scale_log2), ng2 = make_float2(neg, neg);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
             if constexpr (C::kTF32) {
 #pragma unroll
                 for (int c = 0; c < 128; c += 2) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sr[c]), scale_log2, neg));
-                    const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), scale_log2, neg));
-                    sum0 += p0;
-                    sum1 += p1;
-                    sr[c] = __float_as_uint(p0);
-                    sr[c + 1] = __float_as_uint(p1);
+                    const float2 x = fma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2, ng2);
+                    const float2 p = make_float2(ex2(x.x), ex2(x.y));
+                    if ((c >> 1) & 1) acc1 = add2(acc1, p); else acc0 = add2(acc0, p);
+                    sr[c] = __float_as_uint(p.x);
+                    sr[c + 1] = __float_as_uint(p.y);
                 }
                 tmem_st_x128(tSr, sr);
             } else {
                 uint32_t pk[64];
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), scale_log2, neg));
-                    const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, neg));
-                    sum0 += p0;
-                    sum1 += p1;
-                    pk[c] = pack_bf16(p0, p1);
+                for (int u = 0; u < 64; ++u) {
+                    const float2 x =
+                        fma2(make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), sl2, ng2);
+                    const float2 p = make_float2(ex2(x.x), ex2(x.y));
+                    if (u & 1) acc1 = add2(acc1, p); else acc0 = add2(acc0, p);
+                    pk[u] = pack_bf16(p.x, p.y);
                 }
                 tmem_st_x64(tSr, pk);
             }
+            const float2 accs = add2(acc0, acc1);
+            const float sum0 = accs.x, sum1 = accs.y;
             l_run = l_run * alpha + (sum0 + sum1);
             if (j > 0 && __any_sync(0xffffffffu, upd)) {
                 // O still holds sum_{j' < j} P V relative to the old max: rescale it once
