@@ -7,10 +7,10 @@
 // dQ = scale * dS K.
 //
 // Three kernels on the caller's stream:
-//  1. bwd_pre:  D_i = sum_t dO_it O_it (fp32), the logsumexp in base 2 (L * log2 e),
-//               both padded to whole 128-row tiles (padding rows get D = 0 and
-//               L = +inf, so their probabilities are exactly 0), and the fp32 dQ
-//               accumulator cleared.
+//  1. bwd_pre:  D_i = sum_t dO_it O_it (fp32), the negated logsumexp in base 2
+//               (-L * log2 e), both padded to whole 128-row tiles (padding rows get
+//               D = 0 and -L = -inf, so their probabilities are exactly 0), and the
+//               fp32 dQ accumulator cleared.
 //  2. bwd_main: one CTA per (batch*head, 128-key block j).  K_j and V_j stay in
 //               shared memory; the CTA walks the query blocks i (i >= j when causal:
 //               blocks above the diagonal are skipped) and per block runs five
@@ -156,7 +156,7 @@ bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restr
         for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (r < total_rows && part == 0) {
             delta[r] = valid ? acc : 0.f;
-            lse2[r] = valid ? lse[src_row] * kLog2e : INFINITY;
+            lse2[r] = valid ? -lse[src_row] * kLog2e : -INFINITY;
         }
     }
     const long long n4 = static_cast<long long>(BH) * N * D / 4;
@@ -418,15 +418,25 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             {
                 uint32_t sr[128];
                 tmem_ld_x128(tSr, sr);
-                const float *L = Lvec + qs * kTileRows;
+                const float2 *nL = reinterpret_cast<const float2 *>(Lvec + qs * kTileRows);  // -L * log2 e
+                const float2 sl2 = make_float2(scale_log2, scale_log2);
                 // causal: query q sees key c iff c <= q (same block offsets on the diagonal)
                 const int qmin = (causal && i == j) ? c : 0;
+                if (key_valid && qmin == 0) {
 #pragma unroll
-                for (int q = 0; q < 128; q += 2) {
-                    const float e0 = ex2(fmaf(__uint_as_float(sr[q]), scale_log2, -L[q]));
-                    const float e1 = ex2(fmaf(__uint_as_float(sr[q + 1]), scale_log2, -L[q + 1]));
-                    pk[q >> 1] = pack_bf16((key_valid && q >= qmin) ? e0 : 0.f,
-                                           (key_valid && q + 1 >= qmin) ? e1 : 0.f);
+                    for (int u = 0; u < 64; ++u) {
+                        const float2 x = fma2(make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])),
+                                              sl2, nL[u]);
+                        pk[u] = pack_bf16(ex2(x.x), ex2(x.y));
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 64; ++u) {
+                        const float2 x = fma2(make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])),
+                                              sl2, nL[u]);
+                        pk[u] = pack_bf16((key_valid && 2 * u >= qmin) ? ex2(x.x) : 0.f,
+                                          (key_valid && 2 * u + 1 >= qmin) ? ex2(x.y) : 0.f);
+                    }
                 }
             }
             tmem_st_x64(tSr, pk);
@@ -436,7 +446,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDPFull), it & 1, wc, kSiteBSoftDP));
             if (!ok) break;
             tc_fence_after();
-            const float *Dv = Dvec + qs * kTileRows;
+            const float2 *D2 = reinterpret_cast<const float2 *>(Dvec + qs * kTileRows);
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {                 // 32 query columns at a time
                 uint32_t r[32];
@@ -444,11 +454,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 uint32_t dk2[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
-                    const int q0 = 32 * ch + 2 * t;
                     const uint32_t pp = pk[16 * ch + t];
-                    const float p0 = __uint_as_float(pp << 16), p1 = __uint_as_float(pp & 0xffff0000u);
-                    dk2[t] = pack_bf16(p0 * (__uint_as_float(r[2 * t]) - Dv[q0]),
-                                       p1 * (__uint_as_float(r[2 * t + 1]) - Dv[q0 + 1]));
+                    const float2 p = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u));
+                    const float2 ds = mul2(p, sub2(make_float2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1])),
+                                                   D2[16 * ch + t]));
+                    dk2[t] = pack_bf16(ds.x, ds.y);
                 }
                 // shared: query columns 32*ch .. 32*ch+31 = box (ch / 2), 16-byte chunks
                 // 4*(ch % 2) .. 4*(ch % 2)+3 of this key's row

@@ -29,7 +29,7 @@ struct BwdArgs {
     void *dq, *dk, *dv;
     float *dq_acc;      // workspace: [BH, N, d] fp32
     float *delta;       // workspace: [BH, Npad] fp32, D = rowsum(dO o O)
-    float *lse2;        // workspace: [BH, Npad] fp32, logsumexp in base 2 (+inf on padding rows)
+    float *lse2;        // workspace: [BH, Npad] fp32, negated logsumexp in base 2 (-inf on padding rows)
     int N, Npad, BH, d;
     float scale;
     int causal;
