@@ -359,14 +359,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tc_fence_after();
                 mma_tn(tDV, tS, sDO + dos * C::kTileBytes, it > 0);
                 mma_commit(bar(B::kDOEmpty + dos));
-                // S^T for the next query block
+                // S^T for the next query block and dK/dQ for this one are independent
+                // (different TMEM columns); whichever can go first goes first: if dS is
+                // already there, dK and dQ (on the dQ read-out chain) are issued before S.
                 int qs_next = -1;
-                if (it + 1 < n_it) {
+                auto issue_next_s = [&]() -> bool {
                     qs_next = wait_q(it + 1);
-                    if (qs_next < 0) { ok = false; break; }
+                    if (qs_next < 0) return false;
                     mma_kk(tS, sK, sQ + qs_next * C::kTileBytes);
                     mma_commit(bar(B::kSFull));
-                }
+                    return true;
+                };
+                const bool ds_ready = mbar_try_wait(bar(B::kDSFull), it & 1);
+                if (!ds_ready && it + 1 < n_it && !issue_next_s()) { ok = false; break; }
                 // dK += dS^T Q_i ;  dQ_i = dS K_j
                 if (!mbar_wait(bar(B::kDSFull), it & 1, wc, kSiteBMmaDS)) { ok = false; break; }
                 tc_fence_after();
@@ -378,6 +383,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                   sdesc_sw128(sK + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024), C::kIdescDQ,
                                   kk > 0 ? 1u : 0u);
                 mma_commit(bar(B::kDQFull));
+                if (ds_ready && it + 1 < n_it && !issue_next_s()) { ok = false; break; }
                 qs = qs_next;
                 // dP^T for the next query block, once dQ_i has been read out of its columns
                 if (it + 1 < n_it) {
@@ -447,10 +453,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!ok) break;
             tc_fence_after();
             const float2 *D2 = reinterpret_cast<const float2 *>(Dvec + qs * kTileRows);
+            // 32 query columns at a time; the load of the next chunk is in flight while
+            // this chunk is computed and stored
+            uint32_t rbuf[2][32];
+            tmem_ld_x32_nowait(tDPr, rbuf[0]);
+            tmem_wait_ld_fence(rbuf[0]);
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {                 // 32 query columns at a time
-                uint32_t r[32];
-                tmem_ld_x32(tDPr + 32u * ch, r);
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t (&r)[32] = rbuf[ch & 1];
+                if (ch < 3) tmem_ld_x32_nowait(tDPr + 32u * (ch + 1), rbuf[(ch + 1) & 1]);
                 uint32_t dk2[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
@@ -469,8 +480,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     *reinterpret_cast<uint4 *>(box + ((chunk ^ swz) << 4)) =
                         make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
                 }
-                // tensor memory: dS^T packed over the first 64 dP^T columns (these columns
-                // have already been read: chunk ch reads 32ch.., writes 16ch..)
+                // tensor memory: dS^T packed over the first 64 dP^T columns (chunk ch
+                // writes columns 16ch.., all of which have been read by now)
                 asm volatile(
                     "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
                     "%12, %13, %14, %15, %16};\n\t" ::"r"(tDPr + 16u * ch),
@@ -478,6 +489,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     "r"(dk2[6]), "r"(dk2[7]), "r"(dk2[8]), "r"(dk2[9]), "r"(dk2[10]), "r"(dk2[11]),
                     "r"(dk2[12]), "r"(dk2[13]), "r"(dk2[14]), "r"(dk2[15])
                     : "memory");
+                if (ch < 3) tmem_wait_ld_fence(rbuf[(ch + 1) & 1]);
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             fence_proxy_async_smem();
