@@ -144,6 +144,22 @@ def dist_setup(backend):
     return world, rank, local
 
 
+def max_over_ranks(value, device="cpu"):
+    """The slowest rank's value (the job is only as fast as its slowest replica)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, steps, flops_per_rank_step, total_ms):
+    """Whole-job throughput: every rank runs its own replica of the step."""
+    return world * steps * flops_per_rank_step / (total_ms * 1e-3) / 1e12
+
+
 def cpu_oracle_sample(q, k, v, do, d, rows):
     """Time the fp64 oracle (forward + backward) on the listed query rows of every head."""
     import oracle
@@ -254,12 +270,8 @@ def run_ours(args, world, rank, local):
     t_fwd = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
     t_bwd = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     t_step = [a + b for a, b in zip(t_fwd, t_bwd)]
-    total_ms = sum(t_step)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * args.steps * (fwd_flops + bwd_flops) / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(sum(t_step), dev)
+    value = job_tflops(world, args.steps, fwd_flops + bwd_flops, total_ms)
     fwd_tf = fwd_flops / (statistics.mean(t_fwd) * 1e-3) / 1e12
     bwd_tf = bwd_flops / (statistics.mean(t_bwd) * 1e-3) / 1e12
 

@@ -23,7 +23,8 @@ FA_ERR_CUDA = 5
 FA_ERR_DEVICE_TIMEOUT = 6
 
 EXPORTED = ("fa_fwd", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_noalloc",
-            "fa_get_device_status", "fa_status_string", "fa_last_cuda_error")
+            "fa_get_device_status", "fa_selftest_wait_timeout", "fa_status_string",
+            "fa_last_cuda_error")
 NOALLOC_SCRATCH_BYTES = 64 << 20   # FA_NOALLOC_SCRATCH_BYTES in include/fa.h
 
 _lock = threading.Lock()
@@ -60,6 +61,8 @@ def load() -> ctypes.CDLL:
         lib.fa_bwd_noalloc.restype = I
         lib.fa_get_device_status.argtypes = [vp]
         lib.fa_get_device_status.restype = I
+        lib.fa_selftest_wait_timeout.argtypes = [vp]
+        lib.fa_selftest_wait_timeout.restype = I
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_last_cuda_error.argtypes = []

@@ -12,6 +12,7 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "ptx.cuh"
 
 namespace fa {
 namespace {
@@ -21,6 +22,23 @@ namespace {
 __device__ unsigned int g_status_word[2];
 
 thread_local int t_last_cuda_error = 0;
+
+// One warp waits on an mbarrier that nothing ever arrives at.  The bounded wait gives
+// up after its time limit, raises the abort flag and records the timeout in the device
+// status word; the kernel then returns normally, leaving the context usable.
+__global__ void wait_selftest_kernel(unsigned int *status) {
+    __shared__ __align__(8) unsigned long long barrier;
+    __shared__ int abort_flag;
+    const uint32_t bar = smem_u32(&barrier);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const WaitCtx wc{&abort_flag, status};
+    mbar_wait(bar, 0, wc, /*site=*/1);
+}
 
 int cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -244,6 +262,16 @@ extern "C" int fa_get_device_status(fa_stream_t stream) {
         if (e != cudaSuccess) return cuda_fail(e);
         return FA_ERR_DEVICE_TIMEOUT;
     }
+    return FA_OK;
+}
+
+extern "C" int fa_selftest_wait_timeout(fa_stream_t stream) {
+    DeviceState *ds = nullptr;
+    int st = device_state(&ds);
+    if (st != FA_OK) return st;
+    wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(ds->status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
     return FA_OK;
 }
 

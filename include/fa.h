@@ -24,8 +24,8 @@
  *     visible to query i iff j <= i.  causal == 0 attends to all N keys.
  *   - lse holds the natural-log logsumexp of the scaled scores over the visible
  *     keys: lse_i = log(sum_j exp(scale * q_i . k_j)).
- *   - Pointers are device pointers (the _host entry points excepted), 16-byte
- *     aligned (the tensor-memory-access engine needs it); lse 4-byte aligned.
+ *   - Pointers are device pointers, 16-byte aligned (the tensor-memory-access
+ *     engine needs it); lse 4-byte aligned.
  *   - Ownership: the caller allocates and owns every buffer, workspaces
  *     included.  The library allocates no device memory, keeps no state
  *     between calls (beyond per-device one-time set-up) and never synchronises
@@ -98,8 +98,9 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   workspace   device buffer of at least fa_bwd_workspace_size(B,H,N,d)
  *               bytes, 256-byte aligned; its contents on entry do not matter
  *               and are scratch on exit
- * The dQ contributions of different key blocks are summed with fp32 atomic
- * adds, so dq can differ from run to run in the last bits.
+ * The dQ contributions of different key blocks are summed with fp32 bulk
+ * reductions in an order that varies, so dq can differ from run to run in the
+ * last bits; dk and dv are deterministic.
  * Page: "FlashAttention" (deep dive), section "How it works" (backward
  * recomputes P = exp(Q K^T * scale - L), D = rowsum(dO o O),
  * dS = P o (dP - D)); the scale enters dQ and dK by the chain rule.
@@ -139,6 +140,15 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
  * FA_ERR_CUDA if the synchronisation itself failed.
  */
 int fa_get_device_status(fa_stream_t stream);
+
+/*
+ * Failure-detection self-test: enqueues a one-warp kernel on `stream` whose mbarrier
+ * wait nothing ever satisfies.  After the wait's time limit (about one second) the
+ * kernel records FA_ERR_DEVICE_TIMEOUT in the device status word and returns; the CUDA
+ * context stays usable.  Read the result with fa_get_device_status().  Does no other
+ * work.  The pages have no counterpart: this checks the library's own bounded waits.
+ */
+int fa_selftest_wait_timeout(fa_stream_t stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char *fa_status_string(int status);
