@@ -27,7 +27,9 @@
 //
 // Tensor memory (512 columns): dK [0, d) | dV [d, 2d) | S^T [2d, 2d+128) | dP^T [2d+128,
 // 2d+256).  P^T (bf16) is written over the first 64 S^T columns, dS^T over the first 64
-// dP^T columns, and dQ_i accumulates in the dP^T columns once dK has consumed dS^T.
+// dP^T columns, and dQ_i accumulates in the S^T columns once dV has consumed P^T.  Per
+// query block the MMA warp issues dV_i | dQ_i, dK_i | S^T_{i+1} (after the dQ_i read-out)
+// | dP^T_{i+1}: the read-out gates only the next S^T, not the next dP^T.
 //
 // Warp roles (320 threads): warps 0-3 own one key row each (softmax recompute and dS),
 // warps 4-7 own one query row each (dQ read-out, staging and bulk reduce), warp 8
@@ -354,48 +356,40 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mma_commit(bar(B::kDPFull));
             }
             for (int it = 0; ok && it < n_it; ++it) {
-                // dV += P^T dO_i
+                // dV += P^T dO_i (P^T from the S^T columns)
                 if (!mbar_wait(bar(B::kPFull), it & 1, wc, kSiteBMmaP)) { ok = false; break; }
                 tc_fence_after();
                 mma_tn(tDV, tS, sDO + dos * C::kTileBytes, it > 0);
                 mma_commit(bar(B::kDOEmpty + dos));
-                // S^T for the next query block and dK/dQ for this one are independent
-                // (different TMEM columns); whichever can go first goes first: if dS is
-                // already there, dK and dQ (on the dQ read-out chain) are issued before S.
-                int qs_next = -1;
-                auto issue_next_s = [&]() -> bool {
-                    qs_next = wait_q(it + 1);
-                    if (qs_next < 0) return false;
-                    mma_kk(tS, sK, sQ + qs_next * C::kTileBytes);
-                    mma_commit(bar(B::kSFull));
-                    return true;
-                };
-                const bool ds_ready = mbar_try_wait(bar(B::kDSFull), it & 1);
-                if (!ds_ready && it + 1 < n_it && !issue_next_s()) { ok = false; break; }
-                // dK += dS^T Q_i ;  dQ_i = dS K_j
+                // dQ_i = dS K_j into the S^T columns (after dV has read P^T from them), then
+                // dK += dS^T Q_i (dS^T from the dP^T columns)
                 if (!mbar_wait(bar(B::kDSFull), it & 1, wc, kSiteBMmaDS)) { ok = false; break; }
                 tc_fence_after();
-                mma_tn(tDK, tDP, sQ + qs * C::kTileBytes, it > 0);
-                mma_commit(bar(B::kQEmpty + qs));
 #pragma unroll
                 for (int kk = 0; kk < C::kRowSteps; ++kk)
-                    mma_ss<false>(tDP, sdesc_sw128(sDS + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024),
+                    mma_ss<false>(tS, sdesc_sw128(sDS + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024),
                                   sdesc_sw128(sK + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024), C::kIdescDQ,
                                   kk > 0 ? 1u : 0u);
                 mma_commit(bar(B::kDQFull));
-                if (ds_ready && it + 1 < n_it && !issue_next_s()) { ok = false; break; }
-                qs = qs_next;
-                // dP^T for the next query block, once dQ_i has been read out of its columns
+                mma_tn(tDK, tDP, sQ + qs * C::kTileBytes, it > 0);
+                mma_commit(bar(B::kQEmpty + qs));
                 if (it + 1 < n_it) {
+                    // S^T for the next query block, once dQ_i has been read out of the S^T
+                    // columns; then dP^T (its columns are free once dK has read dS^T)
                     if (!mbar_wait(bar(B::kDQFree), it & 1, wc, kSiteBMmaDQ)) { ok = false; break; }
                     tc_fence_after();
+                    qs = wait_q(it + 1);
+                    if (qs < 0) { ok = false; break; }
+                    mma_kk(tS, sK, sQ + qs * C::kTileBytes);
+                    mma_commit(bar(B::kSFull));
                     dos = wait_do(it + 1);
                     if (dos < 0) { ok = false; break; }
                     mma_kk(tDP, sV, sDO + dos * C::kTileBytes);
                     mma_commit(bar(B::kDPFull));
                 }
             }
-            // Drain the tensor pipe before tensor memory can be released.
+            // Drain the tensor pipe before tensor memory can be released; the dK/dV
+            // epilogue waits on the same commit (it follows the last dK product).
             mma_commit(bar(B::kDrain));
             mbar_wait_drain(bar(B::kDrain), 0, wc, kSiteBDrain);
         }
@@ -498,7 +492,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         // ------------------------------------------------------------ epilogue: dV row
         if (ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDQFull), (n_it - 1) & 1, wc, kSiteBEpi));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDrain), 0, wc, kSiteBEpi));
         }
         if (ok) {
             tc_fence_after();
@@ -523,7 +517,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;                   // query row within the block
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tDQr = tmem + lane_off + C::kDPCol;
+        const uint32_t tDQr = tmem + lane_off + C::kSCol;   // dQ_i accumulates in the S^T columns
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int i = i0 + it;
@@ -567,7 +561,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (threadIdx.x == 128) bulk_wait_group0();
         // ------------------------------------------------------------ epilogue: dK row
         if (ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDQFull), (n_it - 1) & 1, wc, kSiteBEpi));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDrain), 0, wc, kSiteBEpi));
         }
         if (ok) {
             tc_fence_after();
