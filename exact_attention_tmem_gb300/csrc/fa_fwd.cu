@@ -36,15 +36,22 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;          // 10 warps
-constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kRescaleBound = 256.0f;    // 2^kRescaleThreshold
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <typename T, int D>
+template <typename T, int D, int QT>
 struct FwdCfg {
     static constexpr bool kTF32 = std::is_same<T, float>::value;
+    // QT query tiles of 128 rows per CTA: 4 softmax warps per tile, then the MMA warp
+    // and the TMA warp.  With QT = 1 two CTAs share an SM (half the shared memory and
+    // tensor memory each); with QT = 2 one CTA owns the SM.
+    static constexpr int kQT = QT;
+    static constexpr int kMmaWarp = 4 * QT;
+    static constexpr int kLoadWarp = 4 * QT + 1;
+    static constexpr int kThreads = 32 * (4 * QT + 2);
+    static constexpr int kMinBlocks = QT == 1 ? 2 : 1;
+    static constexpr int kSmemBudget = QT == 1 ? 100 * 1024 : 200 * 1024;
     static constexpr int kEB = static_cast<int>(sizeof(T));
     static constexpr int kRowBytes = D * kEB;
     static constexpr int kBoxCols = kBoxBytes / kEB;        // elements per 128-byte box row
@@ -54,12 +61,12 @@ struct FwdCfg {
     static constexpr int kKStep = 32 / kEB;                  // K elements per MMA instruction
     static constexpr int kQKSteps = kRowBytes / 32;
     static constexpr int kPVSteps = kTileRows / kKStep;
-    static constexpr int kStagesFit = (200 * 1024 - 2 * kTileBytes) / kTileBytes;
+    static constexpr int kStagesFit = (kSmemBudget - QT * kTileBytes) / kTileBytes;
     // TF32: two stages, so K always lands in stage 0 and V in stage 1 (see kVtOff)
     static constexpr int kStages = kTF32 ? 2 : (kStagesFit > 8 ? 8 : kStagesFit);
     // shared memory map, offsets from a 1024-byte aligned base
     static constexpr int kQOff = 0;
-    static constexpr int kKVOff = 2 * kTileBytes;
+    static constexpr int kKVOff = QT * kTileBytes;
     // TF32 only: V^T of the current V tile, K-major (the TF32 B operand must be K-major):
     // 4 boxes of 32 keys (128 bytes) x D rows.
     static constexpr int kVtOff = kKVOff + kStages * kTileBytes;
@@ -70,8 +77,8 @@ struct FwdCfg {
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     // tensor memory columns
-    static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kOCol = 256;
+    static constexpr uint32_t kTmemCols = QT == 2 ? 512 : 256;
+    static constexpr uint32_t kOCol = 128 * QT;
     static constexpr uint32_t kFmt = kTF32 ? kFormatTF32 : kFormatBF16;
     static constexpr uint32_t kIdescQK = make_idesc(kFmt, 128, 128, false, false);
     static constexpr uint32_t kIdescPV = make_idesc(kFmt, 128, D, false, !kTF32);
@@ -79,7 +86,8 @@ struct FwdCfg {
     static_assert(kRowBytes % kBoxBytes == 0, "row must be whole 128-byte boxes");
     static_assert(kStages >= 2, "need at least two K/V stages");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-    static_assert(256 + 2 * D <= 512, "tensor memory budget");
+    static_assert(128 * QT + QT * D <= kTmemCols, "tensor memory budget");
+    static_assert(!kTF32 || QT == 2, "the TF32 variant keeps two query tiles per CTA");
 };
 
 // barrier indices
@@ -100,12 +108,14 @@ enum : int {
     kSiteSoftO = 16, kSiteEpiO = 17, kSiteDrain = 18, kSiteMmaDrain = 19
 };
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename T, int D, int QT>
+__global__ void __launch_bounds__(FwdCfg<T, D, QT>::kThreads, FwdCfg<T, D, QT>::kMinBlocks)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, T *__restrict__ out, float *__restrict__ lse,
            int N, int num_pairs, float scale_log2, int causal, unsigned int *status) {
-    using C = FwdCfg<T, D>;
+    using C = FwdCfg<T, D, QT>;
+    constexpr int kMmaWarp = C::kMmaWarp;
+    constexpr int kLoadWarp = C::kLoadWarp;
     using B = Bars<C::kStages>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -123,14 +133,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int lane = threadIdx.x & 31;
     const int bh = blockIdx.x / num_pairs;
     const int rank = blockIdx.x % num_pairs;
-    // heaviest pair first within a head when causal
+    // heaviest group of query tiles first within a head when causal
     const int pair = causal ? (num_pairs - 1 - rank) : rank;
     const int nkv = (N + kTileRows - 1) / kTileRows;
     int ntile[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        const int qt = 2 * pair + t;
-        ntile[t] = (qt * kTileRows >= N) ? 0 : (causal ? min(qt + 1, nkv) : nkv);
+        const int qt = QT * pair + t;
+        ntile[t] = (t >= QT || qt * kTileRows >= N) ? 0 : (causal ? min(qt + 1, nkv) : nkv);
     }
     const int nmax = max(ntile[0], ntile[1]);
 
@@ -175,7 +185,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 if (ntile[t] == 0) continue;
                 for (int b = 0; b < C::kBoxes; ++b)
                     tma_load_3d(sQ + t * C::kTileBytes + b * C::kBoxTileBytes, &tm_q, bar(B::kQ),
-                                b * C::kBoxCols, (2 * pair + t) * kTileRows, bh);
+                                b * C::kBoxCols, (QT * pair + t) * kTileRows, bh);
             }
         }
         int seq = 0;
@@ -235,7 +245,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 if (ntile[t] == 0) continue;
                 for (int b = 0; b < C::kBoxes; ++b)
                     tma_load_3d(sQ + t * C::kTileBytes + b * C::kBoxTileBytes, &tm_q, bar(B::kQ),
-                                b * C::kBoxCols, (2 * pair + t) * kTileRows, bh);
+                                b * C::kBoxCols, (QT * pair + t) * kTileRows, bh);
             }
             int seq = 0;
             for (; seq < 2 * nmax; ++seq) {
@@ -339,7 +349,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const int t = warp >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
-        const int row_g = (2 * pair + t) * kTileRows + row;
+        const int row_g = (QT * pair + t) * kTileRows + row;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tSr = tmem + lane_off + 128u * t;
         const uint32_t tOr = tmem + lane_off + C::kOCol + D * t;
@@ -355,32 +365,40 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             // mask: causal (key > query) and keys past N in the last tile
             const int kv0 = j * kTileRows;
             const int lim = min(causal ? row_g - kv0 : kTileRows - 1, N - 1 - kv0);
-            if (lim < kTileRows - 1) {
+            auto apply_mask = [&]() {
+                if (lim < kTileRows - 1) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c > lim) sr[c] = __float_as_uint(-INFINITY);
-            }
-            // row max: four independent chains of three-input max
-            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+                    for (int c = 0; c < 128; ++c)
+                        if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+                }
+            };
+            apply_mask();
+            // Row max of the scaled scores (base-2 units): four chains of three-input max.
+            auto row_max = [&]() -> float {
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 128; c += 8) {
-                mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-                mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-                mx2 = max3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-                mx3 = max3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
-            }
-            const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
+                for (int c = 0; c < 128; c += 8) {
+                    mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                    mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                    mx2 = max3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+                    mx3 = max3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+                }
+                return fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
+            };
+            const float2 sl2 = make_float2(scale_log2, scale_log2);
             float alpha = 1.f;
-            const bool upd = mx > m_run + kRescaleThreshold;
-            if (upd) {
-                alpha = ex2(m_run - mx);
-                m_run = mx;
-            }
-            const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
-            // P = 2^(s * scale_log2 - m): paired FFMA, two EX2, paired sums
-            const float2 sl2 = make_float2(scale_log2, scale_log2), ng2 = make_float2(neg, neg);
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+            bool upd = false;
+            float sum0, sum1;
             if constexpr (C::kTF32) {
+                const float mx = row_max();
+                upd = mx > m_run + kRescaleThreshold;
+                if (upd) {
+                    alpha = ex2(m_run - mx);
+                    m_run = mx;
+                }
+                const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
+                const float2 ng2 = make_float2(neg, neg);
+                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int c = 0; c < 128; c += 2) {
                     const float2 x = fma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2, ng2);
@@ -390,20 +408,81 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     sr[c + 1] = __float_as_uint(p.y);
                 }
                 tmem_st_x128(tSr, sr);
+                const float2 accs = add2(acc0, acc1);
+                sum0 = accs.x;
+                sum1 = accs.y;
             } else {
+                // P = 2^(s * scale_log2 - m) as packed bf16, with paired FFMA and sums.
                 uint32_t pk[64];
+                auto exp_pass = [&](float m) -> float {
+                    const float neg = (m == -INFINITY) ? 0.f : -m;
+                    const float2 ng2 = make_float2(neg, neg);
+                    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int u = 0; u < 64; ++u) {
-                    const float2 x =
-                        fma2(make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), sl2, ng2);
-                    const float2 p = make_float2(ex2(x.x), ex2(x.y));
-                    if (u & 1) acc1 = add2(acc1, p); else acc0 = add2(acc0, p);
-                    pk[u] = pack_bf16(p.x, p.y);
+                    for (int u = 0; u < 64; ++u) {
+                        const float2 x =
+                            fma2(make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), sl2, ng2);
+                        const float2 p = make_float2(ex2(x.x), ex2(x.y));
+                        if (u & 1) acc1 = add2(acc1, p); else acc0 = add2(acc0, p);
+                        pk[u] = pack_bf16(p.x, p.y);
+                    }
+                    const float2 accs = add2(acc0, acc1);
+                    return accs.x + accs.y;
+                };
+                // Fast path: exponentiate against the running max.  A block sum below 2^8
+                // means every P is below 2^8, the bound the lazy rescale allows, so the
+                // row max is not needed.  Otherwise take the max (reading S again from
+                // tensor memory, where it still is) and recompute only if it grew by more
+                // than the threshold.  The first block always starts from the max.
+                float blk;
+                if (__any_sync(0xffffffffu, m_run == -INFINITY)) {
+                    // max first (the first block of every row; kept warp-uniform)
+                    const float mx = row_max();
+                    upd = mx > m_run + (m_run == -INFINITY ? 0.f : kRescaleThreshold);
+                    if (upd) {
+                        alpha = ex2(m_run - mx);
+                        m_run = mx;
+                    }
+                    blk = exp_pass(m_run);
+                } else {
+                    blk = exp_pass(m_run);
+                    // tcgen05.ld is warp-collective: the slow path is taken by the whole
+                    // warp when any of its rows needs it.
+                    if (__any_sync(0xffffffffu, !(blk < kRescaleBound))) {
+                        float m4 = -INFINITY;
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch) {
+                            uint32_t r[32];
+                            tmem_ld_x32(tSr + 32u * ch, r);
+                            float a0 = -INFINITY, a1 = -INFINITY;
+#pragma unroll
+                            for (int c = 0; c < 32; c += 4) {
+                                const int cc = 32 * ch + c;
+                                a0 = max3(a0, cc > lim ? -INFINITY : __uint_as_float(r[c]),
+                                          cc + 1 > lim ? -INFINITY : __uint_as_float(r[c + 1]));
+                                a1 = max3(a1, cc + 2 > lim ? -INFINITY : __uint_as_float(r[c + 2]),
+                                          cc + 3 > lim ? -INFINITY : __uint_as_float(r[c + 3]));
+                            }
+                            m4 = max3(m4, a0, a1);
+                        }
+                        const float mx = m4 * scale_log2;
+                        upd = mx > m_run + kRescaleThreshold;
+                        if (upd) {
+                            alpha = ex2(m_run - mx);
+                            m_run = mx;
+                        }
+                        // Rows whose max did not move recompute exactly the P they had.
+                        if (__any_sync(0xffffffffu, upd)) {
+                            tmem_ld_x128(tSr, sr);
+                            apply_mask();
+                            blk = exp_pass(m_run);
+                        }
+                    }
                 }
                 tmem_st_x64(tSr, pk);
+                sum0 = blk;
+                sum1 = 0.f;
             }
-            const float2 accs = add2(acc0, acc1);
-            const float sum0 = accs.x, sum1 = accs.y;
             l_run = l_run * alpha + (sum0 + sum1);
             if (j > 0 && __any_sync(0xffffffffu, upd)) {
                 // O still holds sum_{j' < j} P V relative to the old max: rescale it once
@@ -475,32 +554,41 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
 }
 
-template <typename T, int D>
+template <typename T, int D, int QT>
 cudaError_t launch_fwd_t(const FwdArgs &a, cudaStream_t stream) {
-    using C = FwdCfg<T, D>;
-    auto kern = fwd_kernel<T, D>;
+    using C = FwdCfg<T, D, QT>;
+    auto kern = fwd_kernel<T, D, QT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int num_pairs = (a.N + 2 * kTileRows - 1) / (2 * kTileRows);
-    const long long blocks = static_cast<long long>(a.BH) * num_pairs;
+    const int group_rows = QT * kTileRows;
+    const int num_groups = (a.N + group_rows - 1) / group_rows;
+    const long long blocks = static_cast<long long>(a.BH) * num_groups;
     if (blocks <= 0 || blocks > INT_MAX) return cudaErrorInvalidValue;
     const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-    kern<<<static_cast<unsigned>(blocks), kThreads, C::kSmemBytes, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, static_cast<T *>(a.o), a.lse, a.N, num_pairs, scale_log2, a.causal,
+    kern<<<static_cast<unsigned>(blocks), C::kThreads, C::kSmemBytes, stream>>>(
+        a.tm_q, a.tm_k, a.tm_v, static_cast<T *>(a.o), a.lse, a.N, num_groups, scale_log2, a.causal,
         a.status);
     return cudaGetLastError();
+}
+
+// bf16 tile policy (measured on GB300): causal work is best served by two query tiles
+// per CTA (the pair 2g, 2g+1 has nearly equal cost); non-causal by one tile per CTA and
+// two CTAs per SM, which gives each tile its own MMA-issuing thread.
+template <int D>
+cudaError_t launch_fwd_bf16_d(const FwdArgs &a, cudaStream_t stream) {
+    return a.causal ? launch_fwd_t<__nv_bfloat16, D, 2>(a, stream) : launch_fwd_t<__nv_bfloat16, D, 1>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdArgs &a, cudaStream_t stream) {
-    if (a.d == 64) return launch_fwd_t<__nv_bfloat16, 64>(a, stream);
-    if (a.d == 128) return launch_fwd_t<__nv_bfloat16, 128>(a, stream);
+    if (a.d == 64) return launch_fwd_bf16_d<64>(a, stream);
+    if (a.d == 128) return launch_fwd_bf16_d<128>(a, stream);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t stream) {
-    if (a.d == 64) return launch_fwd_t<float, 64>(a, stream);
+    if (a.d == 64) return launch_fwd_t<float, 64, 2>(a, stream);
     return cudaErrorInvalidValue;
 }
 
