@@ -42,8 +42,8 @@ REF_STEP_ROWS = 32      # query rows per head per step of the reference arm
 # they had when the counters were taken; after any change it reads as null until the
 # capture is repeated.
 TRAFFIC = {
-    "bwd": (1985.2e6, ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"), "5d3a2caaa7fc57b5"),
-    "fwd": (494.8e6, ("fa_fwd.cu", "ptx.cuh", "fa_internal.h"), "f55f43c6ec16e276"),
+    "bwd": (1985.6e6, ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"), "450695c0097d4576"),
+    "fwd": (495.4e6, ("fa_fwd.cu", "ptx.cuh", "fa_internal.h"), "112083cc9a0bc3e9"),
 }
 
 
