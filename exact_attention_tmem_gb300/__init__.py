@@ -28,47 +28,67 @@ def _stream_ptr(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
-def _check_qkv(dtype, *ts):
-    t0 = ts[0]
-    if t0.dim() != 4:
-        raise ValueError("expected [B, H, N, d] tensors")
+def _check_tensors(dtype, shape, *ts):
     for t in ts:
         if not t.is_cuda:
             raise ValueError("tensors must be CUDA tensors")
         if t.dtype != dtype:
             raise ValueError(f"expected {dtype}, got {t.dtype}")
-        if t.shape != t0.shape:
-            raise ValueError("q, k, v (and o, dO) must share one [B, H, N, d] shape")
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"expected shape {tuple(shape)}, got {tuple(t.shape)}")
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous")
-        if t.device != t0.device:
+        if t.device != ts[0].device:
             raise ValueError("tensors must be on one device")
+
+
+def _shapes(q, k):
+    """[B, H, N, d] queries and [B, Hkv, N, d] keys/values (Hkv divides H)."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    B, H, N, d = q.shape
+    if k.shape[0] != B or k.shape[2] != N or k.shape[3] != d:
+        raise ValueError("q and k/v must agree in B, N and d")
+    Hkv = k.shape[1]
+    if H % Hkv != 0:
+        raise ValueError("the number of query heads must be a multiple of the key/value heads")
+    return B, H, Hkv, N, d
 
 
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
     """O = softmax(scale * q k^T [causal mask]) v and the natural-log logsumexp per row.
 
-    bf16 tensors use fa_fwd; float32 tensors use fa_fwd_f32 (d = 64 only).
+    q: [B, H, N, d]; k, v: [B, Hkv, N, d] with Hkv dividing H (Hkv < H is grouped-query
+    attention: query head h uses key/value head h // (H // Hkv)).  bf16 tensors use
+    fa_fwd / fa_fwd_gqa; float32 tensors use fa_fwd_f32 (d = 64, Hkv = H).
     Returns (o, lse) with lse float32 [B, H, N].
     """
     dtype = q.dtype
     if dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("q, k, v must be bfloat16 or float32")
-    _check_qkv(dtype, q, k, v)
-    B, H, N, d = q.shape
+    B, H, Hkv, N, d = _shapes(q, k)
+    _check_tensors(dtype, q.shape, q)
+    _check_tensors(dtype, k.shape, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    _check_qkv(dtype, q, out)
+    _check_tensors(dtype, q.shape, q, out)
     if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
     lib = _lib.load()
-    fn = lib.fa_fwd if dtype == torch.bfloat16 else lib.fa_fwd_f32
-    st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-            B, H, N, d, scale, int(bool(causal)), _stream_ptr(q.device))
-    _lib.check(st, "fa_fwd" if dtype == torch.bfloat16 else "fa_fwd_f32")
+    stream = _stream_ptr(q.device)
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr())
+    if dtype == torch.float32:
+        if Hkv != H:
+            raise ValueError("grouped-query attention takes bfloat16 tensors")
+        st, name = lib.fa_fwd_f32(*ptrs, B, H, N, d, scale, int(bool(causal)), stream), "fa_fwd_f32"
+    elif Hkv == H:
+        st, name = lib.fa_fwd(*ptrs, B, H, N, d, scale, int(bool(causal)), stream), "fa_fwd"
+    else:
+        st, name = lib.fa_fwd_gqa(*ptrs, B, H, Hkv, N, d, scale, int(bool(causal)), stream), "fa_fwd_gqa"
+    _lib.check(st, name)
     return out, lse
 
 
@@ -78,24 +98,35 @@ def bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
 
 def bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
         dq=None, dk=None, dv=None, workspace=None):
-    """Gradients (dq, dk, dv) of sum(o * do), recomputing the probabilities from lse."""
-    _check_qkv(torch.bfloat16, q, k, v, o, do)
-    B, H, N, d = q.shape
+    """Gradients (dq, dk, dv) of sum(o * do), recomputing the probabilities from lse.
+
+    Shapes as in fwd; with grouped-query attention dk and dv are [B, Hkv, N, d] and sum
+    the contributions of the query heads that share each key/value head.
+    """
+    B, H, Hkv, N, d = _shapes(q, k)
+    _check_tensors(torch.bfloat16, q.shape, q, o, do)
+    _check_tensors(torch.bfloat16, k.shape, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    _check_qkv(torch.bfloat16, q, dq, dk, dv)
+    _check_tensors(torch.bfloat16, q.shape, q, dq)
+    _check_tensors(torch.bfloat16, k.shape, k, dk, dv)
     if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
     need = bwd_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    st = _lib.load().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                            do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                            B, H, N, d, scale, int(bool(causal)), _stream_ptr(q.device))
-    _lib.check(st, "fa_bwd")
+    lib = _lib.load()
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size())
+    stream = _stream_ptr(q.device)
+    if Hkv == H:
+        st, name = lib.fa_bwd(*args, B, H, N, d, scale, int(bool(causal)), stream), "fa_bwd"
+    else:
+        st, name = lib.fa_bwd_gqa(*args, B, H, Hkv, N, d, scale, int(bool(causal)), stream), "fa_bwd_gqa"
+    _lib.check(st, name)
     return dq, dk, dv
 
 

@@ -22,7 +22,8 @@ FA_ERR_WORKSPACE = 4
 FA_ERR_CUDA = 5
 FA_ERR_DEVICE_TIMEOUT = 6
 
-EXPORTED = ("fa_fwd", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_noalloc",
+EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_gqa",
+            "fa_bwd_noalloc",
             "fa_get_device_status", "fa_selftest_wait_timeout", "fa_status_string",
             "fa_last_cuda_error")
 NOALLOC_SCRATCH_BYTES = 64 << 20   # FA_NOALLOC_SCRATCH_BYTES in include/fa.h
@@ -51,12 +52,16 @@ def load() -> ctypes.CDLL:
         vp, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, F, I, vp]
         lib.fa_fwd.restype = I
+        lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, F, I, vp]
+        lib.fa_fwd_gqa.restype = I
         lib.fa_fwd_f32.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, F, I, vp]
         lib.fa_fwd_f32.restype = I
         lib.fa_bwd_workspace_size.argtypes = [I, I, I, I]
         lib.fa_bwd_workspace_size.restype = Z
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, Z, I, I, I, I, F, I, vp]
         lib.fa_bwd.restype = I
+        lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, Z, I, I, I, I, I, F, I, vp]
+        lib.fa_bwd_gqa.restype = I
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, vp]
         lib.fa_bwd_noalloc.restype = I
         lib.fa_get_device_status.argtypes = [vp]

@@ -49,8 +49,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Shape checks shared by every entry point.  Products are formed in 64 bits.
-int check_shape(int B, int H, int N, int d) {
-    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+int check_shape(int B, int H, int N, int d, int Hkv) {
+    if (B < 1 || H < 1 || N < 1 || d < 1 || Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
     const long long bh = static_cast<long long>(B) * H;
     if (bh > INT_MAX) return FA_ERR_INVALID_ARG;
     const long long elems = bh * N;
@@ -136,10 +136,10 @@ int make_tmap(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int eb, i
     return FA_OK;
 }
 
-int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
-               int d, float scale, int causal, cudaStream_t stream, bool f32) {
+int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Hkv,
+               int N, int d, float scale, int causal, cudaStream_t stream, bool f32) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-    int st = check_shape(B, H, N, d);
+    int st = check_shape(B, H, N, d, Hkv);
     if (st != FA_OK) return st;
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (f32 && d != 64) return FA_ERR_UNSUPPORTED;
@@ -152,15 +152,16 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     std::memset(&a, 0, sizeof(a));
     const CUtensorMapDataType dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const int eb = f32 ? 4 : 2;
-    const int BH = B * H;
+    const int BH = B * H, BHkv = B * Hkv;
     if ((st = make_tmap(&a.tm_q, q, dt, eb, d, N, BH)) != FA_OK) return st;
-    if ((st = make_tmap(&a.tm_k, k, dt, eb, d, N, BH)) != FA_OK) return st;
-    if ((st = make_tmap(&a.tm_v, v, dt, eb, d, N, BH)) != FA_OK) return st;
+    if ((st = make_tmap(&a.tm_k, k, dt, eb, d, N, BHkv)) != FA_OK) return st;
+    if ((st = make_tmap(&a.tm_v, v, dt, eb, d, N, BHkv)) != FA_OK) return st;
     a.o = o;
     a.lse = lse;
     a.N = N;
     a.BH = BH;
     a.d = d;
+    a.group = H / Hkv;
     a.scale = scale;
     a.causal = causal ? 1 : 0;
     a.status = ds->status;
@@ -176,18 +177,24 @@ using namespace fa;
 
 extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
                       int d, float scale, int causal, fa_stream_t stream) {
-    return fwd_common(q, k, v, o, lse, B, H, N, d, scale, causal, reinterpret_cast<cudaStream_t>(stream),
+    return fwd_common(q, k, v, o, lse, B, H, H, N, d, scale, causal, reinterpret_cast<cudaStream_t>(stream),
+                      false);
+}
+
+extern "C" int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                          int Hkv, int N, int d, float scale, int causal, fa_stream_t stream) {
+    return fwd_common(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, reinterpret_cast<cudaStream_t>(stream),
                       false);
 }
 
 extern "C" int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse, int B, int H,
                           int N, int d, float scale, int causal, fa_stream_t stream) {
-    return fwd_common(q, k, v, o, lse, B, H, N, d, scale, causal, reinterpret_cast<cudaStream_t>(stream),
+    return fwd_common(q, k, v, o, lse, B, H, H, N, d, scale, causal, reinterpret_cast<cudaStream_t>(stream),
                       true);
 }
 
 extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
-    if (check_shape(B, H, N, d) != FA_OK) return 0;
+    if (check_shape(B, H, N, d, H) != FA_OK) return 0;
     const size_t bh = static_cast<size_t>(B) * H;
     const size_t npad = (static_cast<size_t>(N) + kTileRows - 1) / kTileRows * kTileRows;
     const size_t acc = bh * static_cast<size_t>(N) * d * sizeof(float);
@@ -196,11 +203,13 @@ extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
     return acc_aligned + 2 * vec;
 }
 
-extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                      const void *dout, void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
-                      int B, int H, int N, int d, float scale, int causal, fa_stream_t stream) {
+namespace fa {
+namespace {
+int bwd_common(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
+               void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes, int B, int H, int Hkv,
+               int N, int d, float scale, int causal, fa_stream_t stream) {
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-    int st = check_shape(B, H, N, d);
+    int st = check_shape(B, H, N, d, Hkv);
     if (st != FA_OK) return st;
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
@@ -214,11 +223,11 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
     if (st != FA_OK) return st;
     BwdArgs a;
     std::memset(&a, 0, sizeof(a));
-    const int BH = B * H;
+    const int BH = B * H, BHkv = B * Hkv;
     const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if ((st = make_tmap(&a.tm_q, q, dt, 2, d, N, BH)) != FA_OK) return st;
-    if ((st = make_tmap(&a.tm_k, k, dt, 2, d, N, BH)) != FA_OK) return st;
-    if ((st = make_tmap(&a.tm_v, v, dt, 2, d, N, BH)) != FA_OK) return st;
+    if ((st = make_tmap(&a.tm_k, k, dt, 2, d, N, BHkv)) != FA_OK) return st;
+    if ((st = make_tmap(&a.tm_v, v, dt, 2, d, N, BHkv)) != FA_OK) return st;
     if ((st = make_tmap(&a.tm_do, dout, dt, 2, d, N, BH)) != FA_OK) return st;
     const size_t npad = (static_cast<size_t>(N) + kTileRows - 1) / kTileRows * kTileRows;
     const size_t acc = static_cast<size_t>(BH) * N * d * sizeof(float);
@@ -239,12 +248,29 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
     a.Npad = static_cast<int>(npad);
     a.BH = BH;
     a.d = d;
+    a.group = H / Hkv;
     a.scale = scale;
     a.causal = causal ? 1 : 0;
     a.status = ds->status;
     cudaError_t e = launch_bwd_bf16(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return FA_OK;
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                      const void *dout, void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                      int B, int H, int N, int d, float scale, int causal, fa_stream_t stream) {
+    return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H, H, N, d, scale, causal,
+                      stream);
+}
+
+extern "C" int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                          const void *dout, void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                          int B, int H, int Hkv, int N, int d, float scale, int causal, fa_stream_t stream) {
+    return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal,
+                      stream);
 }
 
 extern "C" int fa_get_device_status(fa_stream_t stream) {

@@ -198,7 +198,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const __grid_constant__ CUtensorMap tm_dq, const float *__restrict__ lse2,
                 const float *__restrict__ delta,
                 __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int N, int Npad, int nkv,
-                float scale, float scale_log2, int causal, unsigned int *status) {
+                int group, float scale, float scale_log2, int causal, unsigned int *status) {
     using C = BwdCfg<D>;
     using B = BwdBars<C::kQStages, C::kDOStages>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -222,11 +222,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / nkv;
+    const int bh = blockIdx.x / nkv;         // key/value head
     const int j = blockIdx.x % nkv;          // key block; j = 0 (the longest walk) first
     const int nq = Npad / kTileRows;
     const int i0 = causal ? j : 0;
-    const int n_it = nq - i0;                // >= 1
+    const int n_q = nq - i0;                 // query blocks per query head (>= 1)
+    // The walk covers the query blocks of every query head that shares this key/value
+    // head (grouped-query attention; group = 1 is plain multi-head attention):
+    // iteration `it` is query head bh*group + it / n_q, query block i0 + it % n_q.
+    const int n_it = group * n_q;
+    auto q_head = [&](int it) { return bh * group + it / n_q; };
+    auto q_block = [&](int it) { return i0 + it % n_q; };
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B::kKV), 1);
@@ -270,17 +276,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tma_load_3d(sK + b * C::kBoxTileBytes, &tm_k, bar(B::kKV), b * 64, j * kTileRows, bh);
                 tma_load_3d(sV + b * C::kBoxTileBytes, &tm_v, bar(B::kKV), b * 64, j * kTileRows, bh);
             }
-            const float *lrow = lse2 + static_cast<int64_t>(bh) * Npad;
-            const float *drow = delta + static_cast<int64_t>(bh) * Npad;
             int q_loads = 0, do_loads = 0;
             for (int it = 0; it < n_it; ++it) {
-                const int i = i0 + it;
+                const int i = q_block(it), hq = q_head(it);
+                const float *lrow = lse2 + static_cast<int64_t>(hq) * Npad;
+                const float *drow = delta + static_cast<int64_t>(hq) * Npad;
                 const int qs = it % C::kQStages, qu = it / C::kQStages;
                 if (qu > 0 && !mbar_wait(bar(B::kQEmpty + qs), (qu - 1) & 1, wc, kSiteBLoadQ)) break;
                 mbar_arrive_expect_tx(bar(B::kQFull + qs), C::kTileBytes + 2 * C::kVecBytes);
                 for (int b = 0; b < C::kBoxes; ++b)
                     tma_load_3d(sQ + qs * C::kTileBytes + b * C::kBoxTileBytes, &tm_q, bar(B::kQFull + qs),
-                                b * 64, i * kTileRows, bh);
+                                b * 64, i * kTileRows, hq);
                 bulk_load(sL + qs * C::kVecBytes, lrow + i * kTileRows, C::kVecBytes, bar(B::kQFull + qs));
                 bulk_load(sD + qs * C::kVecBytes, drow + i * kTileRows, C::kVecBytes, bar(B::kQFull + qs));
                 ++q_loads;
@@ -289,7 +295,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive_expect_tx(bar(B::kDOFull + ds), C::kTileBytes);
                 for (int b = 0; b < C::kBoxes; ++b)
                     tma_load_3d(sDO + ds * C::kTileBytes + b * C::kBoxTileBytes, &tm_do, bar(B::kDOFull + ds),
-                                b * 64, i * kTileRows, bh);
+                                b * 64, i * kTileRows, hq);
                 ++do_loads;
             }
             // Every copy issued above must land before this CTA may exit: wait for the
@@ -406,7 +412,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int swz = c & 7;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            const int i = i0 + it;
+            const int i = q_block(it);
             const int qs = it % C::kQStages;
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kSFull), it & 1, wc, kSiteBSoftS) &&
                                              mbar_wait(bar(B::kQFull + qs), (it / C::kQStages) & 1, wc, kSiteBSoftL));
@@ -520,7 +526,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t tDQr = tmem + lane_off + C::kSCol;   // dQ_i accumulates in the S^T columns
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            const int i = i0 + it;
+            const int i = q_block(it);
             // all 128 threads leave together, so none is left waiting at a named barrier
             ok = named_barrier_and(1, 128, mbar_wait(bar(B::kDQFull), it & 1, wc, kSiteBDQ));
             if (!ok) break;
@@ -551,7 +557,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                     for (int b = 0; b < 2; ++b)
                         tma_reduce_add_3d(&tm_dq, sDQ + b * C::kBoxTileBytes, pass * C::kDQHalfCols + 32 * b,
-                                          i * kTileRows, bh);
+                                          i * kTileRows, q_head(it));
                     bulk_commit_group();
                     bulk_wait_group_read0();
                 }
@@ -616,12 +622,12 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int nkv = a.Npad / kTileRows;
-    const long long blocks = static_cast<long long>(a.BH) * nkv;
+    const long long blocks = static_cast<long long>(a.BH / a.group) * nkv;
     if (blocks <= 0 || blocks > INT_MAX) return cudaErrorInvalidValue;
     const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     kern<<<static_cast<unsigned>(blocks), kThreads, C::kSmemBytes, stream>>>(
         a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.lse2, a.delta, static_cast<__nv_bfloat16 *>(a.dk),
-        static_cast<__nv_bfloat16 *>(a.dv), a.N, a.Npad, nkv, a.scale, scale_log2, a.causal, a.status);
+        static_cast<__nv_bfloat16 *>(a.dv), a.N, a.Npad, nkv, a.group, a.scale, scale_log2, a.causal, a.status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 

@@ -112,7 +112,7 @@ template <typename T, int D, int QT>
 __global__ void __launch_bounds__(FwdCfg<T, D, QT>::kThreads, FwdCfg<T, D, QT>::kMinBlocks)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, T *__restrict__ out, float *__restrict__ lse,
-           int N, int num_pairs, float scale_log2, int causal, unsigned int *status) {
+           int N, int num_pairs, int group, float scale_log2, int causal, unsigned int *status) {
     using C = FwdCfg<T, D, QT>;
     constexpr int kMmaWarp = C::kMmaWarp;
     constexpr int kLoadWarp = C::kLoadWarp;
@@ -132,6 +132,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int bh = blockIdx.x / num_pairs;
+    // grouped-query attention: `group` query heads share one key/value head
+    const int bh_kv = bh / group;
     const int rank = blockIdx.x % num_pairs;
     // heaviest group of query tiles first within a head when causal
     const int pair = causal ? (num_pairs - 1 - rank) : rank;
@@ -200,7 +202,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     const CUtensorMap *m = (seq & 1) ? &tm_v : &tm_k;
                     for (int b = 0; b < C::kBoxes; ++b)
                         tma_load_3d(sKV + s * C::kTileBytes + b * C::kBoxTileBytes, m, bar(B::kKVFull + s),
-                                    b * C::kBoxCols, (seq >> 1) * kTileRows, bh);
+                                    b * C::kBoxCols, (seq >> 1) * kTileRows, bh_kv);
                 }
             }
             if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
@@ -257,7 +259,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 const int j = seq >> 1;
                 for (int b = 0; b < C::kBoxes; ++b)
                     tma_load_3d(sKV + s * C::kTileBytes + b * C::kBoxTileBytes, m, bar(B::kKVFull + s),
-                                b * C::kBoxCols, j * kTileRows, bh);
+                                b * C::kBoxCols, j * kTileRows, bh_kv);
             }
             // Every copy issued above must land before this CTA may exit.
             mbar_wait_drain(bar(B::kQ), 0, wc, kSiteDrain);
@@ -566,8 +568,8 @@ cudaError_t launch_fwd_t(const FwdArgs &a, cudaStream_t stream) {
     if (blocks <= 0 || blocks > INT_MAX) return cudaErrorInvalidValue;
     const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     kern<<<static_cast<unsigned>(blocks), C::kThreads, C::kSmemBytes, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, static_cast<T *>(a.o), a.lse, a.N, num_groups, scale_log2, a.causal,
-        a.status);
+        a.tm_q, a.tm_k, a.tm_v, static_cast<T *>(a.o), a.lse, a.N, num_groups, a.group, scale_log2,
+        a.causal, a.status);
     return cudaGetLastError();
 }
 

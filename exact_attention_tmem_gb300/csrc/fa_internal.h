@@ -16,6 +16,7 @@ struct FwdArgs {
     void *o;
     float *lse;
     int N, BH, d;
+    int group;             // query heads per key/value head (1: plain multi-head attention)
     float scale;
     int causal;
     unsigned int *status;  // device status word
@@ -30,7 +31,8 @@ struct BwdArgs {
     float *dq_acc;      // workspace: [BH, N, d] fp32
     float *delta;       // workspace: [BH, Npad] fp32, D = rowsum(dO o O)
     float *lse2;        // workspace: [BH, Npad] fp32, negated logsumexp in base 2 (-inf on padding rows)
-    int N, Npad, BH, d;
+    int N, Npad, BH, d;   // BH counts query heads
+    int group;            // query heads per key/value head; B*H/group key/value heads
     float scale;
     int causal;
     unsigned int *status;

@@ -52,7 +52,7 @@ typedef struct CUstream_st *fa_stream_t;
 
 typedef enum fa_status {
     FA_OK = 0,
-    FA_ERR_INVALID_ARG = 1,     /* NULL pointer, B/H/N < 1, non-finite scale, size overflow */
+    FA_ERR_INVALID_ARG = 1,     /* NULL pointer, B/H/N < 1, H not a multiple of Hkv, non-finite scale, size overflow */
     FA_ERR_UNSUPPORTED = 2,     /* d not supported, or the device is not compute capability 10.3 */
     FA_ERR_ALIGNMENT = 3,       /* a pointer is not 16-byte aligned (lse: 4-byte) */
     FA_ERR_WORKSPACE = 4,       /* workspace NULL or smaller than fa_bwd_workspace_size() */
@@ -72,6 +72,17 @@ typedef enum fa_status {
  */
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
+
+/*
+ * Grouped-query forward (GQA; multi-query attention when Hkv = 1): H query heads
+ * share Hkv key/value heads, query head h reading key/value head h / (H / Hkv).
+ *   q, o  [B,H,N,d] bf16;  k, v  [B,Hkv,N,d] bf16;  lse [B,H,N] fp32
+ *   H must be a multiple of Hkv (else FA_ERR_INVALID_ARG).  fa_fwd is Hkv = H.
+ * Page: "FlashAttention" (deep dive), section "Implementation notes" (several query
+ * heads map to one key/value head; the loads are shared and nothing else changes).
+ */
+int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
+               int B, int H, int Hkv, int N, int d, float scale, int causal, fa_stream_t stream);
 
 /*
  * Forward pass with float32 inputs and outputs (same layout and meaning as
@@ -109,6 +120,16 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            const void *dout, void *dq, void *dk, void *dv, void *workspace,
            size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
            fa_stream_t stream);
+
+/*
+ * Grouped-query backward: as fa_bwd, with k, v, dk, dv [B,Hkv,N,d]; dk and dv sum
+ * the contributions of all H / Hkv query heads that share each key/value head.
+ * The workspace is fa_bwd_workspace_size(B, H, N, d) (per query head).
+ */
+int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const float *lse,
+               const void *dout, void *dq, void *dk, void *dv, void *workspace,
+               size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale,
+               int causal, fa_stream_t stream);
 
 /* Size in bytes of the scratch array built into the library for fa_bwd_noalloc. */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)

@@ -151,3 +151,19 @@ def test_python_binding_raises_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         _lib.load()
+
+
+@pytest.mark.parametrize("H,Hkv", [(8, 3), (4, 0), (4, -1), (2, 4)])
+def test_gqa_head_counts_checked(lib, H, Hkv):
+    st = lib.fa_fwd_gqa(A, A, A, A, A, 1, H, Hkv, 128, 128, ctypes.c_float(0.1), 1, None)
+    assert st == _lib.FA_ERR_INVALID_ARG
+    ws = lib.fa_bwd_workspace_size(1, H, 128, 128) or (1 << 20)
+    st = lib.fa_bwd_gqa(*([A] * 9), W, ws, 1, H, Hkv, 128, 128, ctypes.c_float(0.1), 1, None)
+    assert st == _lib.FA_ERR_INVALID_ARG
+
+
+def test_gqa_valid_heads_pass_host_checks(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.fa_fwd_gqa(A, A, A, A, A, 1, 8, 2, 128, 128, ctypes.c_float(0.1), 1, None) == _lib.FA_ERR_CUDA
