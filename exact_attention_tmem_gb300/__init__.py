@@ -16,7 +16,8 @@ import torch
 from . import _lib
 from ._lib import FaError  # noqa: F401
 
-__all__ = ["fwd", "bwd", "bwd_workspace_size", "device_status", "build", "FaError"]
+__all__ = ["fwd", "bwd", "bwd_workspace_size", "bwd_deterministic_workspace_size", "device_status", "build",
+           "FaError"]
 
 
 def build(force: bool = False) -> str:
@@ -96,12 +97,18 @@ def bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(_lib.load().fa_bwd_workspace_size(B, H, N, d))
 
 
+def bwd_deterministic_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(_lib.load().fa_bwd_deterministic_workspace_size(B, H, N, d))
+
+
 def bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
-        dq=None, dk=None, dv=None, workspace=None):
+        dq=None, dk=None, dv=None, workspace=None, deterministic: bool = False):
     """Gradients (dq, dk, dv) of sum(o * do), recomputing the probabilities from lse.
 
     Shapes as in fwd; with grouped-query attention dk and dv are [B, Hkv, N, d] and sum
     the contributions of the query heads that share each key/value head.
+    ``deterministic=True`` uses fa_bwd_deterministic: bit-identical results from run
+    to run (dQ has one writer per row).
     """
     B, H, Hkv, N, d = _shapes(q, k)
     _check_tensors(torch.bfloat16, q.shape, q, o, do)
@@ -114,7 +121,7 @@ def bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
     _check_tensors(torch.bfloat16, k.shape, k, dk, dv)
     if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
-    need = bwd_workspace_size(B, H, N, d)
+    need = (bwd_deterministic_workspace_size if deterministic else bwd_workspace_size)(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     lib = _lib.load()
@@ -122,7 +129,10 @@ def bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
             workspace.numel() * workspace.element_size())
     stream = _stream_ptr(q.device)
-    if Hkv == H:
+    if deterministic:
+        st, name = (lib.fa_bwd_deterministic(*args, B, H, Hkv, N, d, scale, int(bool(causal)), stream),
+                    "fa_bwd_deterministic")
+    elif Hkv == H:
         st, name = lib.fa_bwd(*args, B, H, N, d, scale, int(bool(causal)), stream), "fa_bwd"
     else:
         st, name = lib.fa_bwd_gqa(*args, B, H, Hkv, N, d, scale, int(bool(causal)), stream), "fa_bwd_gqa"

@@ -203,11 +203,19 @@ extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
     return acc_aligned + 2 * vec;
 }
 
+extern "C" size_t fa_bwd_deterministic_workspace_size(int B, int H, int N, int d) {
+    if (check_shape(B, H, N, d, H) != FA_OK) return 0;
+    const size_t bh = static_cast<size_t>(B) * H;
+    const size_t npad = (static_cast<size_t>(N) + kTileRows - 1) / kTileRows * kTileRows;
+    const size_t vec = (bh * npad * sizeof(float) + 255) / 256 * 256;
+    return 2 * vec;
+}
+
 namespace fa {
 namespace {
 int bwd_common(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
                void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes, int B, int H, int Hkv,
-               int N, int d, float scale, int causal, fa_stream_t stream) {
+               int N, int d, float scale, int causal, bool deterministic, fa_stream_t stream) {
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     int st = check_shape(B, H, N, d, Hkv);
     if (st != FA_OK) return st;
@@ -215,7 +223,8 @@ int bwd_common(const void *q, const void *k, const void *v, const void *o, const
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
         !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return FA_ERR_ALIGNMENT;
-    const size_t need = fa_bwd_workspace_size(B, H, N, d);
+    const size_t need = deterministic ? fa_bwd_deterministic_workspace_size(B, H, N, d)
+                                      : fa_bwd_workspace_size(B, H, N, d);
     if (workspace == nullptr || workspace_bytes < need) return FA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGNMENT;
     DeviceState *ds = nullptr;
@@ -231,17 +240,20 @@ int bwd_common(const void *q, const void *k, const void *v, const void *o, const
     if ((st = make_tmap(&a.tm_do, dout, dt, 2, d, N, BH)) != FA_OK) return st;
     const size_t npad = (static_cast<size_t>(N) + kTileRows - 1) / kTileRows * kTileRows;
     const size_t acc = static_cast<size_t>(BH) * N * d * sizeof(float);
-    const size_t acc_aligned = (acc + 255) / 256 * 256;
+    // the deterministic backward keeps no dQ accumulator: the workspace holds only D and L2
+    const size_t acc_aligned = deterministic ? 0 : (acc + 255) / 256 * 256;
     const size_t vec = (static_cast<size_t>(BH) * npad * sizeof(float) + 255) / 256 * 256;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    if ((st = make_tmap(&a.tm_dq, ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH)) != FA_OK) return st;
+    if (!deterministic &&
+        (st = make_tmap(&a.tm_dq, ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH)) != FA_OK)
+        return st;
     a.o = o;
     a.dout = dout;
     a.lse = lse;
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
-    a.dq_acc = reinterpret_cast<float *>(ws);
+    a.dq_acc = deterministic ? nullptr : reinterpret_cast<float *>(ws);
     a.delta = reinterpret_cast<float *>(ws + acc_aligned);
     a.lse2 = reinterpret_cast<float *>(ws + acc_aligned + vec);
     a.N = N;
@@ -251,6 +263,7 @@ int bwd_common(const void *q, const void *k, const void *v, const void *o, const
     a.group = H / Hkv;
     a.scale = scale;
     a.causal = causal ? 1 : 0;
+    a.deterministic = deterministic ? 1 : 0;
     a.status = ds->status;
     cudaError_t e = launch_bwd_bf16(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
@@ -263,14 +276,22 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
                       const void *dout, void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
                       int B, int H, int N, int d, float scale, int causal, fa_stream_t stream) {
     return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H, H, N, d, scale, causal,
-                      stream);
+                      false, stream);
 }
 
 extern "C" int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const float *lse,
                           const void *dout, void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
                           int B, int H, int Hkv, int N, int d, float scale, int causal, fa_stream_t stream) {
     return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal,
-                      stream);
+                      false, stream);
+}
+
+extern "C" int fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                                    const void *dout, void *dq, void *dk, void *dv, void *workspace,
+                                    size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale,
+                                    int causal, fa_stream_t stream) {
+    return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal,
+                      true, stream);
 }
 
 extern "C" int fa_get_device_status(fa_stream_t stream) {

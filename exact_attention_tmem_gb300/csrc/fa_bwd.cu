@@ -161,6 +161,7 @@ bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restr
             lse2[r] = valid ? -lse[src_row] * kLog2e : -INFINITY;
         }
     }
+    if (dq_acc == nullptr) return;   // the deterministic backward has no accumulator
     const long long n4 = static_cast<long long>(BH) * N * D / 4;
     const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -191,7 +192,10 @@ bwd_post_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq
 // ------------------------------------------------------------------------------------
 // 2. main kernel
 // ------------------------------------------------------------------------------------
-template <int D>
+// kDQ = false: the key-block kernel of the deterministic backward, which computes dK and
+// dV only (dQ comes from bwd_dq_kernel); per query block the MMA warp then issues
+// dV_i | S^T_{i+1} | dK_i | dP^T_{i+1}, and dS is not staged in shared memory.
+template <int D, bool kDQ>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -270,7 +274,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_do);
-            tma_prefetch_desc(&tm_dq);
+            if constexpr (kDQ) tma_prefetch_desc(&tm_dq);
             mbar_arrive_expect_tx(bar(B::kKV), 2 * C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b) {
                 tma_load_3d(sK + b * C::kBoxTileBytes, &tm_k, bar(B::kKV), b * 64, j * kTileRows, bh);
@@ -361,37 +365,64 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mma_kk(tDP, sV, sDO + dos * C::kTileBytes);
                 mma_commit(bar(B::kDPFull));
             }
-            for (int it = 0; ok && it < n_it; ++it) {
-                // dV += P^T dO_i (P^T from the S^T columns)
-                if (!mbar_wait(bar(B::kPFull), it & 1, wc, kSiteBMmaP)) { ok = false; break; }
-                tc_fence_after();
-                mma_tn(tDV, tS, sDO + dos * C::kTileBytes, it > 0);
-                mma_commit(bar(B::kDOEmpty + dos));
-                // dQ_i = dS K_j into the S^T columns (after dV has read P^T from them), then
-                // dK += dS^T Q_i (dS^T from the dP^T columns)
-                if (!mbar_wait(bar(B::kDSFull), it & 1, wc, kSiteBMmaDS)) { ok = false; break; }
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < C::kRowSteps; ++kk)
-                    mma_ss<false>(tS, sdesc_sw128(sDS + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024),
-                                  sdesc_sw128(sK + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024), C::kIdescDQ,
-                                  kk > 0 ? 1u : 0u);
-                mma_commit(bar(B::kDQFull));
-                mma_tn(tDK, tDP, sQ + qs * C::kTileBytes, it > 0);
-                mma_commit(bar(B::kQEmpty + qs));
-                if (it + 1 < n_it) {
-                    // S^T for the next query block, once dQ_i has been read out of the S^T
-                    // columns; then dP^T (its columns are free once dK has read dS^T)
-                    if (!mbar_wait(bar(B::kDQFree), it & 1, wc, kSiteBMmaDQ)) { ok = false; break; }
+            if constexpr (kDQ) {
+                for (int it = 0; ok && it < n_it; ++it) {
+                    // dV += P^T dO_i (P^T from the S^T columns)
+                    if (!mbar_wait(bar(B::kPFull), it & 1, wc, kSiteBMmaP)) { ok = false; break; }
                     tc_fence_after();
-                    qs = wait_q(it + 1);
-                    if (qs < 0) { ok = false; break; }
-                    mma_kk(tS, sK, sQ + qs * C::kTileBytes);
-                    mma_commit(bar(B::kSFull));
-                    dos = wait_do(it + 1);
-                    if (dos < 0) { ok = false; break; }
-                    mma_kk(tDP, sV, sDO + dos * C::kTileBytes);
-                    mma_commit(bar(B::kDPFull));
+                    mma_tn(tDV, tS, sDO + dos * C::kTileBytes, it > 0);
+                    mma_commit(bar(B::kDOEmpty + dos));
+                    // dQ_i = dS K_j into the S^T columns (after dV has read P^T from them), then
+                    // dK += dS^T Q_i (dS^T from the dP^T columns)
+                    if (!mbar_wait(bar(B::kDSFull), it & 1, wc, kSiteBMmaDS)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < C::kRowSteps; ++kk)
+                        mma_ss<false>(tS, sdesc_sw128(sDS + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024),
+                                      sdesc_sw128(sK + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024), C::kIdescDQ,
+                                      kk > 0 ? 1u : 0u);
+                    mma_commit(bar(B::kDQFull));
+                    mma_tn(tDK, tDP, sQ + qs * C::kTileBytes, it > 0);
+                    mma_commit(bar(B::kQEmpty + qs));
+                    if (it + 1 < n_it) {
+                        // S^T for the next query block, once dQ_i has been read out of the S^T
+                        // columns; then dP^T (its columns are free once dK has read dS^T)
+                        if (!mbar_wait(bar(B::kDQFree), it & 1, wc, kSiteBMmaDQ)) { ok = false; break; }
+                        tc_fence_after();
+                        qs = wait_q(it + 1);
+                        if (qs < 0) { ok = false; break; }
+                        mma_kk(tS, sK, sQ + qs * C::kTileBytes);
+                        mma_commit(bar(B::kSFull));
+                        dos = wait_do(it + 1);
+                        if (dos < 0) { ok = false; break; }
+                        mma_kk(tDP, sV, sDO + dos * C::kTileBytes);
+                        mma_commit(bar(B::kDPFull));
+                    }
+                }
+            } else {
+                for (int it = 0; ok && it < n_it; ++it) {
+                    if (!mbar_wait(bar(B::kPFull), it & 1, wc, kSiteBMmaP)) { ok = false; break; }
+                    tc_fence_after();
+                    mma_tn(tDV, tS, sDO + dos * C::kTileBytes, it > 0);
+                    mma_commit(bar(B::kDOEmpty + dos));
+                    int qs_next = -1;
+                    if (it + 1 < n_it) {  // S^T_{i+1}: the S^T columns are free after dV_i
+                        qs_next = wait_q(it + 1);
+                        if (qs_next < 0) { ok = false; break; }
+                        mma_kk(tS, sK, sQ + qs_next * C::kTileBytes);
+                        mma_commit(bar(B::kSFull));
+                    }
+                    if (!mbar_wait(bar(B::kDSFull), it & 1, wc, kSiteBMmaDS)) { ok = false; break; }
+                    tc_fence_after();
+                    mma_tn(tDK, tDP, sQ + qs * C::kTileBytes, it > 0);
+                    mma_commit(bar(B::kQEmpty + qs));
+                    qs = qs_next;
+                    if (it + 1 < n_it) {  // dP^T_{i+1}: its columns are free after dK_i
+                        dos = wait_do(it + 1);
+                        if (dos < 0) { ok = false; break; }
+                        mma_kk(tDP, sV, sDO + dos * C::kTileBytes);
+                        mma_commit(bar(B::kDPFull));
+                    }
                 }
             }
             // Drain the tensor pipe before tensor memory can be released; the dK/dV
@@ -472,13 +503,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     dk2[t] = pack_bf16(ds.x, ds.y);
                 }
                 // shared: query columns 32*ch .. 32*ch+31 = box (ch / 2), 16-byte chunks
-                // 4*(ch % 2) .. 4*(ch % 2)+3 of this key's row
-                uint8_t *box = ds_row0 + (ch >> 1) * C::kBoxTileBytes;
+                // 4*(ch % 2) .. 4*(ch % 2)+3 of this key's row (only the dQ product reads it)
+                if constexpr (kDQ) {
+                    uint8_t *box = ds_row0 + (ch >> 1) * C::kBoxTileBytes;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int chunk = 4 * (ch & 1) + u;
-                    *reinterpret_cast<uint4 *>(box + ((chunk ^ swz) << 4)) =
-                        make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
+                    for (int u = 0; u < 4; ++u) {
+                        const int chunk = 4 * (ch & 1) + u;
+                        *reinterpret_cast<uint4 *>(box + ((chunk ^ swz) << 4)) =
+                            make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
+                    }
                 }
                 // tensor memory: dS^T packed over the first 64 dP^T columns (chunk ch
                 // writes columns 16ch.., all of which have been read by now)
@@ -525,7 +558,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tDQr = tmem + lane_off + C::kSCol;   // dQ_i accumulates in the S^T columns
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
+        for (int it = 0; kDQ && it < n_it; ++it) {
             const int i = q_block(it);
             // all 128 threads leave together, so none is left waiting at a named barrier
             ok = named_barrier_and(1, 128, mbar_wait(bar(B::kDQFull), it & 1, wc, kSiteBDQ));
@@ -601,6 +634,374 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
+// ------------------------------------------------------------------------------------
+// 4. query-block kernel of the deterministic backward: dQ with one writer per row
+// ------------------------------------------------------------------------------------
+// One CTA per (query head, pair of 128-row query tiles), the forward kernel's layout:
+// Q_t and dO_t of both tiles stay in shared memory while K_j and V_j stream through
+// their own rings (two K stages, so K_{j+1} is resident while dQ_t(j) still reads
+// K_j).  Per key block j and tile t the tensor cores compute
+//     S_t  = Q_t K_j^T           (TMEM, SD_t columns)   -> P = 2^(S*scale*log2e - L2)
+//     dP_t = dO_t V_j^T          (TMEM, the same columns once S has been read)
+//     dQ_t += dS_t K_j           (A = dS_t, packed bf16 over the first 64 SD_t columns)
+// and dQ_t accumulates in TMEM across the whole walk in key-block order, so the
+// result is the same bits on every run.  dQ = scale * dQ_t is written once.
+// Tensor memory: SD_0 [0,128) | SD_1 [128,256) | dQ_0 [256,256+d) | dQ_1 [256+d,256+2d).
+template <int D>
+struct DqCfg {
+    static constexpr int kBoxes = D * 2 / kBoxBytes;
+    static constexpr int kBoxTileBytes = kTileRows * kBoxBytes;
+    static constexpr int kTileBytes = kBoxes * kBoxTileBytes;
+    static constexpr int kKStages = 2;
+    static constexpr int kVStages = D == 128 ? 1 : 2;
+    static constexpr int kQOff = 0;                          // Q_0, Q_1
+    static constexpr int kDOOff = 2 * kTileBytes;            // dO_0, dO_1
+    static constexpr int kKOff = 4 * kTileBytes;
+    static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 8 + 1;
+    static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+    static constexpr int kSmemBytes = kMiscOff + 16;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kDQCol = 256;
+    static constexpr int kKSteps = D / 16;
+    static constexpr int kRowSteps = kTileRows / 16;
+    static constexpr uint32_t kIdescS = make_idesc(kFormatBF16, 128, 128, false, false);
+    static constexpr uint32_t kIdescDQ = make_idesc(kFormatBF16, 128, D, false, true);
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(256 + 2 * D <= 512, "tensor memory budget");
+};
+
+template <int KS, int VS>
+struct DqBars {
+    static constexpr int kQ = 0;
+    static constexpr int kKFull = 1;                  // + stage
+    static constexpr int kKEmpty = 1 + KS;            // + stage
+    static constexpr int kVFull = 1 + 2 * KS;         // + stage
+    static constexpr int kVEmpty = 1 + 2 * KS + VS;   // + stage
+    static constexpr int kSFull = 1 + 2 * KS + 2 * VS;  // + tile
+    static constexpr int kSRead = kSFull + 2;         // + tile
+    static constexpr int kDPFull = kSFull + 4;        // + tile
+    static constexpr int kDSFull = kSFull + 6;        // + tile
+    static constexpr int kDone = kSFull + 8;
+};
+
+enum : int {
+    kSiteQLoadK = 51, kSiteQLoadV = 52, kSiteQMmaQ = 53, kSiteQMmaK = 54, kSiteQMmaV = 55, kSiteQMmaS = 56,
+    kSiteQMmaDS = 57, kSiteQSoftS = 58, kSiteQSoftDP = 59, kSiteQEpi = 60, kSiteQDrain = 61,
+    kSiteQMisaligned = 62
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+              const float *__restrict__ lse2, const float *__restrict__ delta, __nv_bfloat16 *__restrict__ dq,
+              int N, int Npad, int num_pairs, int group, float scale, float scale_log2, int causal,
+              unsigned int *status) {
+    using C = DqCfg<D>;
+    using B = DqBars<C::kKStages, C::kVStages>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = smem_u32(smem_raw);
+    if ((base & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned window
+        if (threadIdx.x == 0 && atomicOr(&status[0], kStatusTimeout) == 0u) status[1] = kSiteQMisaligned;
+        return;
+    }
+    uint8_t *smem = smem_raw;
+    const uint32_t sQ = base + C::kQOff, sDO = base + C::kDOOff;
+    const uint32_t sK = base + C::kKOff, sV = base + C::kVOff, sBar = base + C::kBarOff;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
+    const WaitCtx wc{abort_flag, status};
+    auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / num_pairs;            // query head
+    const int bh_kv = bh / group;                     // its key/value head
+    const int rank = blockIdx.x % num_pairs;
+    const int pair = causal ? (num_pairs - 1 - rank) : rank;   // longest walks first
+    const int nkv = (N + kTileRows - 1) / kTileRows;
+    int ntile[2];                                     // key blocks each query tile visits
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int qt = 2 * pair + t;
+        ntile[t] = qt * kTileRows >= N ? 0 : (causal ? min(qt + 1, nkv) : nkv);
+    }
+    const int nmax = max(ntile[0], ntile[1]);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B::kQ), 1);
+        for (int s = 0; s < C::kKStages; ++s) {
+            mbar_init(bar(B::kKFull + s), 1);
+            mbar_init(bar(B::kKEmpty + s), 1);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
+            mbar_init(bar(B::kVFull + s), 1);
+            mbar_init(bar(B::kVEmpty + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(B::kSFull + t), 1);
+            mbar_init(bar(B::kSRead + t), 128);
+            mbar_init(bar(B::kDPFull + t), 1);
+            mbar_init(bar(B::kDSFull + t), 128);
+        }
+        mbar_init(bar(B::kDone), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kLoadWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_do);
+            uint32_t qbytes = 0;
+            for (int t = 0; t < 2; ++t) qbytes += ntile[t] > 0 ? 2 * C::kTileBytes : 0;
+            mbar_arrive_expect_tx(bar(B::kQ), qbytes);
+            for (int t = 0; t < 2; ++t) {
+                if (ntile[t] == 0) continue;
+                for (int b = 0; b < C::kBoxes; ++b) {
+                    tma_load_3d(sQ + t * C::kTileBytes + b * C::kBoxTileBytes, &tm_q, bar(B::kQ), b * 64,
+                                (2 * pair + t) * kTileRows, bh);
+                    tma_load_3d(sDO + t * C::kTileBytes + b * C::kBoxTileBytes, &tm_do, bar(B::kQ), b * 64,
+                                (2 * pair + t) * kTileRows, bh);
+                }
+            }
+            int k_loads = 0, v_loads = 0;
+            for (int j = 0; j < nmax; ++j) {
+                const int ks = j % C::kKStages, ku = j / C::kKStages;
+                if (ku > 0 && !mbar_wait(bar(B::kKEmpty + ks), (ku - 1) & 1, wc, kSiteQLoadK)) break;
+                mbar_arrive_expect_tx(bar(B::kKFull + ks), C::kTileBytes);
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_load_3d(sK + ks * C::kTileBytes + b * C::kBoxTileBytes, &tm_k, bar(B::kKFull + ks), b * 64,
+                                j * kTileRows, bh_kv);
+                ++k_loads;
+                const int vs = j % C::kVStages, vu = j / C::kVStages;
+                if (vu > 0 && !mbar_wait(bar(B::kVEmpty + vs), (vu - 1) & 1, wc, kSiteQLoadV)) break;
+                mbar_arrive_expect_tx(bar(B::kVFull + vs), C::kTileBytes);
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_load_3d(sV + vs * C::kTileBytes + b * C::kBoxTileBytes, &tm_v, bar(B::kVFull + vs), b * 64,
+                                j * kTileRows, bh_kv);
+                ++v_loads;
+            }
+            // Every copy issued above must land before this CTA may exit.
+            mbar_wait_drain(bar(B::kQ), 0, wc, kSiteQDrain);
+            for (int s = 0; s < C::kKStages && s < k_loads; ++s) {
+                const int last = s + ((k_loads - 1 - s) / C::kKStages) * C::kKStages;
+                mbar_wait_drain(bar(B::kKFull + s), (last / C::kKStages) & 1, wc, kSiteQDrain);
+            }
+            for (int s = 0; s < C::kVStages && s < v_loads; ++s) {
+                const int last = s + ((v_loads - 1 - s) / C::kVStages) * C::kVStages;
+                mbar_wait_drain(bar(B::kVFull + s), (last / C::kVStages) & 1, wc, kSiteQDrain);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t tSD[2] = {tmem, tmem + 128u};
+            const uint32_t tDQ[2] = {tmem + C::kDQCol, tmem + C::kDQCol + D};
+            auto active = [&](int t, int j) { return j < ntile[t]; };
+            // S_t = A_t B^T over the head dim; A_t = Q_t or dO_t, B = K_j or V_j (both K-major)
+            auto mma_rows = [&](uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile) {
+#pragma unroll
+                for (int kk = 0; kk < C::kKSteps; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32;
+                    mma_ss<false>(d_tmem, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(b_tile + off, 16, 1024),
+                                  C::kIdescS, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto wait_k = [&](int j) -> int {
+                const int s = j % C::kKStages;
+                if (!mbar_wait(bar(B::kKFull + s), (j / C::kKStages) & 1, wc, kSiteQMmaK)) return -1;
+                tc_fence_after();
+                return s;
+            };
+            auto wait_v = [&](int j) -> int {
+                const int s = j % C::kVStages;
+                if (!mbar_wait(bar(B::kVFull + s), (j / C::kVStages) & 1, wc, kSiteQMmaV)) return -1;
+                tc_fence_after();
+                return s;
+            };
+            // dP_t(j) for both tiles once their S has been read; then V_j's stage is free
+            auto issue_dp = [&](int j) -> bool {
+                const int vs = wait_v(j);
+                if (vs < 0) return false;
+                for (int t = 0; t < 2; ++t) {
+                    if (!active(t, j)) continue;
+                    if (!mbar_wait(bar(B::kSRead + t), j & 1, wc, kSiteQMmaS)) return false;
+                    tc_fence_after();
+                    mma_rows(tSD[t], sDO + t * C::kTileBytes, sV + vs * C::kTileBytes);
+                    mma_commit(bar(B::kDPFull + t));
+                }
+                mma_commit(bar(B::kVEmpty + vs));
+                return true;
+            };
+            bool ok = nmax > 0 && mbar_wait(bar(B::kQ), 0, wc, kSiteQMmaQ);
+            if (ok) {
+                tc_fence_after();
+                int ks = wait_k(0);
+                ok = ks >= 0;
+                if (ok) {
+                    for (int t = 0; t < 2; ++t) {
+                        if (!active(t, 0)) continue;
+                        mma_rows(tSD[t], sQ + t * C::kTileBytes, sK + ks * C::kTileBytes);
+                        mma_commit(bar(B::kSFull + t));
+                    }
+                    ok = issue_dp(0);
+                }
+            }
+            for (int j = 0; ok && j < nmax; ++j) {
+                const int ks = j % C::kKStages;
+                int ks_next = -1;
+                for (int t = 0; ok && t < 2; ++t) {
+                    if (!active(t, j)) continue;
+                    // dQ_t += dS_t K_j, then S_t for the next key block into the same columns
+                    if (!mbar_wait(bar(B::kDSFull + t), j & 1, wc, kSiteQMmaDS)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < C::kRowSteps; ++kk)
+                        mma_ts<false>(tDQ[t], tSD[t] + kk * 8u,
+                                      sdesc_sw128(sK + ks * C::kTileBytes + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024),
+                                      C::kIdescDQ, (j > 0 || kk > 0) ? 1u : 0u);
+                    if (active(t, j + 1)) {
+                        if (ks_next < 0) ks_next = wait_k(j + 1);
+                        if (ks_next < 0) { ok = false; break; }
+                        mma_rows(tSD[t], sQ + t * C::kTileBytes, sK + ks_next * C::kTileBytes);
+                        mma_commit(bar(B::kSFull + t));
+                    }
+                }
+                if (!ok) break;
+                mma_commit(bar(B::kKEmpty + ks));
+                if (j + 1 < nmax) ok = issue_dp(j + 1);
+            }
+            // Both tiles' dQ are complete once everything issued so far has retired.
+            mma_commit(bar(B::kDone));
+            mbar_wait_drain(bar(B::kDone), 0, wc, kSiteQDrain);
+        }
+    } else {
+        // ------------------------------------------------------------ query rows (warps 0-7)
+        const int t = warp >> 2;                            // query tile of this warpgroup
+        const int r = (warp & 3) * 32 + lane;               // row within the tile
+        const int qt = 2 * pair + t;
+        const int q = qt * kTileRows + r;                   // query index (< Npad)
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tSDr = tmem + lane_off + 128u * t;
+        const uint32_t tDQr = tmem + lane_off + C::kDQCol + D * t;
+        const int n_j = ntile[t];
+        float nL = 0.f, Dr = 0.f;
+        if (n_j > 0) {
+            nL = lse2[static_cast<int64_t>(bh) * Npad + q];   // -L * log2 e (-inf on padding rows)
+            Dr = delta[static_cast<int64_t>(bh) * Npad + q];
+        }
+        const float2 nL2 = make_float2(nL, nL), D2 = make_float2(Dr, Dr);
+        const float2 sl2 = make_float2(scale_log2, scale_log2);
+        bool ok = true;
+        for (int j = 0; j < n_j; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kSFull + t), j & 1, wc, kSiteQSoftS));
+            if (!ok) break;
+            tc_fence_after();
+            // P = 2^(S * scale*log2e - L2), kept as packed bf16 in registers
+            uint32_t pk[64];
+            {
+                uint32_t sr[128];
+                tmem_ld_x128(tSDr, sr);
+                // keys past N, and (causal) keys after this query, get probability 0
+                const int kmax = min(N - 1 - j * kTileRows, causal ? q - j * kTileRows : kTileRows - 1);
+                if (kmax >= kTileRows - 1) {
+#pragma unroll
+                    for (int u = 0; u < 64; ++u) {
+                        const float2 x = fma2(make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])),
+                                              sl2, nL2);
+                        pk[u] = pack_bf16(ex2(x.x), ex2(x.y));
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 64; ++u) {
+                        const float2 x = fma2(make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])),
+                                              sl2, nL2);
+                        pk[u] = pack_bf16(2 * u <= kmax ? ex2(x.x) : 0.f, 2 * u + 1 <= kmax ? ex2(x.y) : 0.f);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(B::kSRead + t));
+            // dS = P o (dP - D), packed bf16 over the first 64 columns
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDPFull + t), j & 1, wc, kSiteQSoftDP));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t rbuf[2][32];
+            tmem_ld_x32_nowait(tSDr, rbuf[0]);
+            tmem_wait_ld_fence(rbuf[0]);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t (&rr)[32] = rbuf[ch & 1];
+                if (ch < 3) tmem_ld_x32_nowait(tSDr + 32u * (ch + 1), rbuf[(ch + 1) & 1]);
+                uint32_t d2[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const uint32_t pp = pk[16 * ch + u];
+                    const float2 p = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u));
+                    const float2 ds = mul2(p, sub2(make_float2(__uint_as_float(rr[2 * u]), __uint_as_float(rr[2 * u + 1])),
+                                                   D2));
+                    d2[u] = pack_bf16(ds.x, ds.y);
+                }
+                // chunk ch writes columns 16ch .. 16ch+15, all of which have been read
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                    "%12, %13, %14, %15, %16};\n\t" ::"r"(tSDr + 16u * ch),
+                    "r"(d2[0]), "r"(d2[1]), "r"(d2[2]), "r"(d2[3]), "r"(d2[4]), "r"(d2[5]), "r"(d2[6]), "r"(d2[7]),
+                    "r"(d2[8]), "r"(d2[9]), "r"(d2[10]), "r"(d2[11]), "r"(d2[12]), "r"(d2[13]), "r"(d2[14]),
+                    "r"(d2[15])
+                    : "memory");
+                if (ch < 3) tmem_wait_ld_fence(rbuf[(ch + 1) & 1]);
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive(bar(B::kDSFull + t));
+        }
+        // ------------------------------------------------------------ epilogue: dQ row
+        if (ok && n_j > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDone), 0, wc, kSiteQEpi));
+        if (ok && n_j > 0) {
+            tc_fence_after();
+            __nv_bfloat16 *row = dq + (static_cast<int64_t>(bh) * N + (q < N ? q : 0)) * D;
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t v[32];
+                tmem_ld_x32(tDQr + 32u * ch, v);
+                if (q < N) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(row + 32 * ch);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        dst[u] = make_uint4(
+                            pack_bf16(__uint_as_float(v[8 * u]) * scale, __uint_as_float(v[8 * u + 1]) * scale),
+                            pack_bf16(__uint_as_float(v[8 * u + 2]) * scale, __uint_as_float(v[8 * u + 3]) * scale),
+                            pack_bf16(__uint_as_float(v[8 * u + 4]) * scale, __uint_as_float(v[8 * u + 5]) * scale),
+                            pack_bf16(__uint_as_float(v[8 * u + 6]) * scale, __uint_as_float(v[8 * u + 7]) * scale));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
 int grid_for(long long work_items, int per_block) {
     long long g = (work_items + per_block - 1) / per_block;
     if (g < 1) g = 1;
@@ -618,7 +1019,7 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    auto kern = bwd_main_kernel<D>;
+    auto kern = a.deterministic ? bwd_main_kernel<D, false> : bwd_main_kernel<D, true>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int nkv = a.Npad / kTileRows;
@@ -630,6 +1031,20 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
         static_cast<__nv_bfloat16 *>(a.dv), a.N, a.Npad, nkv, a.group, a.scale, scale_log2, a.causal, a.status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+
+    if (a.deterministic) {
+        using CQ = DqCfg<D>;
+        auto qkern = bwd_dq_kernel<D>;
+        e = cudaFuncSetAttribute(qkern, cudaFuncAttributeMaxDynamicSharedMemorySize, CQ::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        const int num_pairs = (nkv + 1) / 2;
+        const long long qblocks = static_cast<long long>(a.BH) * num_pairs;
+        if (qblocks > INT_MAX) return cudaErrorInvalidValue;
+        qkern<<<static_cast<unsigned>(qblocks), kThreads, CQ::kSmemBytes, stream>>>(
+            a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, static_cast<__nv_bfloat16 *>(a.dq), a.N, a.Npad,
+            num_pairs, a.group, a.scale, scale_log2, a.causal, a.status);
+        return cudaGetLastError();
+    }
 
     const long long n8 = static_cast<long long>(a.BH) * a.N * D / 8;
     bwd_post_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(a.dq_acc, static_cast<__nv_bfloat16 *>(a.dq), n8,

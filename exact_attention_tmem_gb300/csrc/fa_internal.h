@@ -28,13 +28,14 @@ struct BwdArgs {
     const void *o, *dout;
     const float *lse;
     void *dq, *dk, *dv;
-    float *dq_acc;      // workspace: [BH, N, d] fp32
+    float *dq_acc;      // workspace: [BH, N, d] fp32 (null for the deterministic backward)
     float *delta;       // workspace: [BH, Npad] fp32, D = rowsum(dO o O)
     float *lse2;        // workspace: [BH, Npad] fp32, negated logsumexp in base 2 (-inf on padding rows)
     int N, Npad, BH, d;   // BH counts query heads
     int group;            // query heads per key/value head; B*H/group key/value heads
     float scale;
     int causal;
+    int deterministic;    // 1: dQ from the query-block kernel (one writer per row), no accumulator
     unsigned int *status;
 };
 

@@ -131,6 +131,33 @@ int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const
                size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale,
                int causal, fa_stream_t stream);
 
+/*
+ * Workspace bytes fa_bwd_deterministic needs for [B,H,N,d] queries (two fp32
+ * vectors per query head, padded to whole 128-row tiles), or 0 if the arguments
+ * are invalid.  Smaller than fa_bwd_workspace_size: there is no dQ accumulator.
+ */
+size_t fa_bwd_deterministic_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Deterministic backward pass: the same gradients as fa_bwd_gqa (Hkv = H for plain
+ * multi-head attention), bit-identical from run to run.  Each dQ row has a single
+ * writer that sums the key blocks in a fixed order, so no reduction across thread
+ * blocks is involved; dK and dV are computed per key block as in fa_bwd.  The
+ * price is recomputing S and dP in the dQ pass (seven tile products per
+ * query/key block pair instead of five).
+ *   q, k, v, o, lse, dout, dq, dk, dv  as for fa_bwd_gqa
+ *   workspace   device buffer of at least fa_bwd_deterministic_workspace_size(B,H,N,d)
+ *               bytes, 256-byte aligned; scratch
+ * Same status codes as fa_bwd.
+ * Page: "FlashAttention" (deep dive), section "How it works" (the backward pass:
+ * recompute P from the saved L, D = rowsum(dO o O), dS = P o (dP - D)); the pages do
+ * not fix how dQ is summed across key blocks.
+ */
+int fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                         void *workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                         int N, int d, float scale, int causal, fa_stream_t stream);
+
 /* Size in bytes of the scratch array built into the library for fa_bwd_noalloc. */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 

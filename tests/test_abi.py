@@ -167,3 +167,44 @@ def test_gqa_valid_heads_pass_host_checks(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert lib.fa_fwd_gqa(A, A, A, A, A, 1, 8, 2, 128, 128, ctypes.c_float(0.1), 1, None) == _lib.FA_ERR_CUDA
+
+
+def bwd_det(lib, ptrs=None, ws=W, ws_bytes=None, B=1, H=2, Hkv=1, N=128, d=128, scale=0.1):
+    p = [A] * 9 if ptrs is None else ptrs
+    if ws_bytes is None:
+        ws_bytes = lib.fa_bwd_deterministic_workspace_size(B, H, N, d) if B > 0 and H > 0 and N > 0 else 0
+    return lib.fa_bwd_deterministic(*p, ws, ws_bytes, B, H, Hkv, N, d, ctypes.c_float(scale), 1, None)
+
+
+def test_deterministic_workspace_size(lib):
+    B, H, N, d = 2, 3, 300, 64
+    vec = -(-(B * H * 384 * 4) // 256) * 256
+    assert lib.fa_bwd_deterministic_workspace_size(B, H, N, d) == 2 * vec
+    assert lib.fa_bwd_deterministic_workspace_size(B, H, N, d) < lib.fa_bwd_workspace_size(B, H, N, d)
+    assert lib.fa_bwd_deterministic_workspace_size(0, 1, 8, 64) == 0
+    assert lib.fa_bwd_deterministic_workspace_size(1, 1, 8, 96) == 0
+
+
+@pytest.mark.parametrize("which", range(9))
+def test_deterministic_null_pointer(lib, which):
+    ptrs = [A] * 9
+    ptrs[which] = None
+    assert bwd_det(lib, ptrs) == _lib.FA_ERR_INVALID_ARG
+
+
+def test_deterministic_host_checks(lib):
+    assert bwd_det(lib, ws=None) == _lib.FA_ERR_WORKSPACE
+    need = lib.fa_bwd_deterministic_workspace_size(1, 2, 128, 128)
+    assert bwd_det(lib, ws_bytes=need - 1) == _lib.FA_ERR_WORKSPACE
+    assert bwd_det(lib, ws=W + 16) == _lib.FA_ERR_ALIGNMENT
+    assert bwd_det(lib, ptrs=[A] * 8 + [A + 8]) == _lib.FA_ERR_ALIGNMENT
+    assert bwd_det(lib, Hkv=3) == _lib.FA_ERR_INVALID_ARG
+    assert bwd_det(lib, d=96, ws_bytes=1 << 30) == _lib.FA_ERR_UNSUPPORTED
+    assert bwd_det(lib, scale=float("inf")) == _lib.FA_ERR_INVALID_ARG
+
+
+def test_deterministic_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert bwd_det(lib) == _lib.FA_ERR_CUDA
