@@ -50,30 +50,34 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+// kDQ = false (the dK/dV-only kernel) needs neither the dS tile nor the dQ staging
+// tile, and spends the room on a third Q stage and a second dO stage, so that the
+// loads run far enough ahead to hide their latency.  The base-2 logsumexp and D of
+// query block i have their own ring of two slots: they are read until dS_i is done.
+template <int D, bool kDQ>
 struct BwdCfg {
     static constexpr int kBoxes = D * 2 / kBoxBytes;
     static constexpr int kBoxTileBytes = kTileRows * kBoxBytes;    // 16 KB
     static constexpr int kTileBytes = kBoxes * kBoxTileBytes;
-    static constexpr int kQStages = 2;
-    static constexpr int kDOStages = (D == 128) ? 1 : 2;
+    static constexpr int kQStages = kDQ ? 2 : 3;
+    static constexpr int kDOStages = (D == 128 && kDQ) ? 1 : 2;
+    static constexpr int kVecStages = 2;
     static constexpr int kVecBytes = kTileRows * 4;                 // 128 fp32
-    static constexpr int kDSBytes = 2 * kBoxTileBytes;              // 128 x 128 bf16
+    static constexpr int kDSBytes = kDQ ? 2 * kBoxTileBytes : 0;    // 128 x 128 bf16
     static constexpr int kDQHalfCols = 64;                          // fp32 columns per staging pass
     static constexpr int kDQPasses = D / kDQHalfCols;
-    static constexpr int kDQStageBytes = kTileRows * kDQHalfCols * 4; // 32 KB = 2 boxes of 32 fp32
+    static constexpr int kDQStageBytes = kDQ ? kTileRows * kDQHalfCols * 4 : 0; // 32 KB = 2 boxes of 32 fp32
     // shared memory map (offsets from a 1024-byte aligned base)
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kKOff + kTileBytes;
     static constexpr int kQOff = kVOff + kTileBytes;
     static constexpr int kDOOff = kQOff + kQStages * kTileBytes;
     static constexpr int kDSOff = kDOOff + kDOStages * kTileBytes;
-    // the base-2 logsumexp and D of query block i travel with Q_i (one stage)
     static constexpr int kDQOff = kDSOff + kDSBytes;
     static constexpr int kLOff = kDQOff + kDQStageBytes;
-    static constexpr int kDOff = kLOff + kQStages * kVecBytes;
-    static constexpr int kBarOff = kDOff + kQStages * kVecBytes;
-    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 7;
+    static constexpr int kDOff = kLOff + kVecStages * kVecBytes;
+    static constexpr int kBarOff = kDOff + kVecStages * kVecBytes;
+    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + kVecStages + 7;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16;
     // tensor memory
@@ -92,14 +96,15 @@ struct BwdCfg {
     static_assert(2 * D + 256 <= 512, "tensor memory budget");
 };
 
-template <int QS, int DS>
+template <int QS, int DS, int VS>
 struct BwdBars {
     static constexpr int kKV = 0;
     static constexpr int kQFull = 1;                 // + stage
     static constexpr int kQEmpty = 1 + QS;           // + stage
     static constexpr int kDOFull = 1 + 2 * QS;       // + stage
     static constexpr int kDOEmpty = 1 + 2 * QS + DS; // + stage
-    static constexpr int kSFull = 1 + 2 * QS + 2 * DS;
+    static constexpr int kVecFull = 1 + 2 * QS + 2 * DS;  // + slot
+    static constexpr int kSFull = 1 + 2 * QS + 2 * DS + VS;
     static constexpr int kDPFull = kSFull + 1;
     static constexpr int kPFull = kSFull + 2;
     static constexpr int kDSFull = kSFull + 3;
@@ -203,8 +208,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const float *__restrict__ delta,
                 __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int N, int Npad, int nkv,
                 int group, float scale, float scale_log2, int causal, unsigned int *status) {
-    using C = BwdCfg<D>;
-    using B = BwdBars<C::kQStages, C::kDOStages>;
+    using C = BwdCfg<D, kDQ>;
+    using B = BwdBars<C::kQStages, C::kDOStages, C::kVecStages>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     if ((base & 1023u) != 0) {  // see the note at the top of this file
@@ -248,6 +253,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(bar(B::kDOFull + s), 1);
             mbar_init(bar(B::kDOEmpty + s), 1);
         }
+        for (int s = 0; s < C::kVecStages; ++s) mbar_init(bar(B::kVecFull + s), 1);
         mbar_init(bar(B::kSFull), 1);
         mbar_init(bar(B::kDPFull), 1);
         mbar_init(bar(B::kPFull), 128);
@@ -280,20 +286,29 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tma_load_3d(sK + b * C::kBoxTileBytes, &tm_k, bar(B::kKV), b * 64, j * kTileRows, bh);
                 tma_load_3d(sV + b * C::kBoxTileBytes, &tm_v, bar(B::kKV), b * 64, j * kTileRows, bh);
             }
-            int q_loads = 0, do_loads = 0;
+            int q_loads = 0, do_loads = 0, vec_loads = 0;
             for (int it = 0; it < n_it; ++it) {
                 const int i = q_block(it), hq = q_head(it);
                 const float *lrow = lse2 + static_cast<int64_t>(hq) * Npad;
                 const float *drow = delta + static_cast<int64_t>(hq) * Npad;
                 const int qs = it % C::kQStages, qu = it / C::kQStages;
                 if (qu > 0 && !mbar_wait(bar(B::kQEmpty + qs), (qu - 1) & 1, wc, kSiteBLoadQ)) break;
-                mbar_arrive_expect_tx(bar(B::kQFull + qs), C::kTileBytes + 2 * C::kVecBytes);
+                mbar_arrive_expect_tx(bar(B::kQFull + qs), C::kTileBytes);
                 for (int b = 0; b < C::kBoxes; ++b)
                     tma_load_3d(sQ + qs * C::kTileBytes + b * C::kBoxTileBytes, &tm_q, bar(B::kQFull + qs),
                                 b * 64, i * kTileRows, hq);
-                bulk_load(sL + qs * C::kVecBytes, lrow + i * kTileRows, C::kVecBytes, bar(B::kQFull + qs));
-                bulk_load(sD + qs * C::kVecBytes, drow + i * kTileRows, C::kVecBytes, bar(B::kQFull + qs));
                 ++q_loads;
+                // the vectors of block it - kVecStages are free once dK of that block (the
+                // end of its dS phase) has been issued and completed
+                const int vs = it % C::kVecStages;
+                if (it >= C::kVecStages) {
+                    const int r = it - C::kVecStages;
+                    if (!mbar_wait(bar(B::kQEmpty + r % C::kQStages), (r / C::kQStages) & 1, wc, kSiteBLoadQ)) break;
+                }
+                mbar_arrive_expect_tx(bar(B::kVecFull + vs), 2 * C::kVecBytes);
+                bulk_load(sL + vs * C::kVecBytes, lrow + i * kTileRows, C::kVecBytes, bar(B::kVecFull + vs));
+                bulk_load(sD + vs * C::kVecBytes, drow + i * kTileRows, C::kVecBytes, bar(B::kVecFull + vs));
+                ++vec_loads;
                 const int ds = it % C::kDOStages, du = it / C::kDOStages;
                 if (du > 0 && !mbar_wait(bar(B::kDOEmpty + ds), (du - 1) & 1, wc, kSiteBLoadDO)) break;
                 mbar_arrive_expect_tx(bar(B::kDOFull + ds), C::kTileBytes);
@@ -313,21 +328,29 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int last = s + ((do_loads - 1 - s) / C::kDOStages) * C::kDOStages;
                 mbar_wait_drain(bar(B::kDOFull + s), (last / C::kDOStages) & 1, wc, kSiteBDrain);
             }
+            for (int s = 0; s < C::kVecStages && s < vec_loads; ++s) {
+                const int last = s + ((vec_loads - 1 - s) / C::kVecStages) * C::kVecStages;
+                mbar_wait_drain(bar(B::kVecFull + s), (last / C::kVecStages) & 1, wc, kSiteBDrain);
+            }
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this loop (every wait is warp-uniform) and lane 0 issues.
+        {
+            auto mbar_wait_w = [&](uint32_t b, uint32_t parity, int site) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
+            };
             const uint32_t tDK = tmem + C::kDKCol, tDV = tmem + C::kDVCol;
             const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDPCol;
             auto wait_q = [&](int it) -> int {
                 const int s = it % C::kQStages;
-                if (!mbar_wait(bar(B::kQFull + s), (it / C::kQStages) & 1, wc, kSiteBMmaQ)) return -1;
+                if (!mbar_wait_w(bar(B::kQFull + s), (it / C::kQStages) & 1, kSiteBMmaQ)) return -1;
                 tc_fence_after();
                 return s;
             };
             auto wait_do = [&](int it) -> int {
                 const int s = it % C::kDOStages;
-                if (!mbar_wait(bar(B::kDOFull + s), (it / C::kDOStages) & 1, wc, kSiteBMmaDO)) return -1;
+                if (!mbar_wait_w(bar(B::kDOFull + s), (it / C::kDOStages) & 1, kSiteBMmaDO)) return -1;
                 tc_fence_after();
                 return s;
             };
@@ -336,7 +359,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int kk = 0; kk < C::kKSteps; ++kk) {
                     const uint32_t off = (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32;
-                    mma_ss<false>(d_tmem, sdesc_sw128(a_s + off, 16, 1024), sdesc_sw128(b_s + off, 16, 1024),
+                    umma_ss(d_tmem, sdesc_sw128(a_s + off, 16, 1024), sdesc_sw128(b_s + off, 16, 1024),
                                   C::kIdescSS, kk > 0 ? 1u : 0u);
                 }
             };
@@ -344,11 +367,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             auto mma_tn = [&](uint32_t d_tmem, uint32_t a_tmem, uint32_t b_s, bool acc) {
 #pragma unroll
                 for (int kk = 0; kk < C::kRowSteps; ++kk)
-                    mma_ts<false>(d_tmem, a_tmem + kk * 8u,
+                    umma_ts(d_tmem, a_tmem + kk * 8u,
                                   sdesc_sw128(b_s + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024), C::kIdescTS,
                                   (acc || kk > 0) ? 1u : 0u);
             };
-            bool ok = mbar_wait(bar(B::kKV), 0, wc, kSiteBMmaKV);
+            bool ok = mbar_wait_w(bar(B::kKV), 0, kSiteBMmaKV);
             tc_fence_after();
             int qs = -1, dos = -1;
             if (ok) {
@@ -357,77 +380,99 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             if (ok) {
                 mma_kk(tS, sK, sQ + qs * C::kTileBytes);
-                mma_commit(bar(B::kSFull));
+                umma_commit(bar(B::kSFull));
                 dos = wait_do(0);
                 ok = dos >= 0;
             }
             if (ok) {
                 mma_kk(tDP, sV, sDO + dos * C::kTileBytes);
-                mma_commit(bar(B::kDPFull));
+                umma_commit(bar(B::kDPFull));
             }
             if constexpr (kDQ) {
+                // dQ_i accumulates in the dP^T columns once dK_i has consumed dS^T from
+                // them.  Per query block: dK_i | dQ_i | dV_{i+1} | dP^T_{i+1} (after the
+                // dQ_i read-out) | S^T_{i+2}, so the read-out overlaps dV_{i+1} and the
+                // softmax warps compute P_{i+1} while dK_i and dQ_i run.
+                if (ok) {  // dV_0, then S^T_1
+                    ok = mbar_wait_w(bar(B::kPFull), 0, kSiteBMmaP);
+                    if (ok) {
+                        tc_fence_after();
+                        mma_tn(tDV, tS, sDO + dos * C::kTileBytes, false);
+                        umma_commit(bar(B::kDOEmpty + dos));     // dP^T_0 and dV_0 have read dO_0
+                    }
+                    if (ok && n_it > 1) {
+                        const int qn = wait_q(1);
+                        ok = qn >= 0;
+                        if (ok) {
+                            mma_kk(tS, sK, sQ + qn * C::kTileBytes);
+                            umma_commit(bar(B::kSFull));
+                        }
+                    }
+                }
                 for (int it = 0; ok && it < n_it; ++it) {
-                    // dV += P^T dO_i (P^T from the S^T columns)
-                    if (!mbar_wait(bar(B::kPFull), it & 1, wc, kSiteBMmaP)) { ok = false; break; }
+                    const int qs_it = it % C::kQStages;
+                    // dK += dS^T Q_i (dS^T from the dP^T columns), then dQ_i = dS K_j
+                    // (dS from shared memory) into the same columns
+                    if (!mbar_wait_w(bar(B::kDSFull), it & 1, kSiteBMmaDS)) { ok = false; break; }
                     tc_fence_after();
-                    mma_tn(tDV, tS, sDO + dos * C::kTileBytes, it > 0);
-                    mma_commit(bar(B::kDOEmpty + dos));
-                    // dQ_i = dS K_j into the S^T columns (after dV has read P^T from them), then
-                    // dK += dS^T Q_i (dS^T from the dP^T columns)
-                    if (!mbar_wait(bar(B::kDSFull), it & 1, wc, kSiteBMmaDS)) { ok = false; break; }
-                    tc_fence_after();
+                    mma_tn(tDK, tDP, sQ + qs_it * C::kTileBytes, it > 0);
+                    umma_commit(bar(B::kQEmpty + qs_it));
 #pragma unroll
                     for (int kk = 0; kk < C::kRowSteps; ++kk)
-                        mma_ss<false>(tS, sdesc_sw128(sDS + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024),
+                        umma_ss(tDP, sdesc_sw128(sDS + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024),
                                       sdesc_sw128(sK + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024), C::kIdescDQ,
                                       kk > 0 ? 1u : 0u);
-                    mma_commit(bar(B::kDQFull));
-                    mma_tn(tDK, tDP, sQ + qs * C::kTileBytes, it > 0);
-                    mma_commit(bar(B::kQEmpty + qs));
+                    umma_commit(bar(B::kDQFull));
                     if (it + 1 < n_it) {
-                        // S^T for the next query block, once dQ_i has been read out of the S^T
-                        // columns; then dP^T (its columns are free once dK has read dS^T)
-                        if (!mbar_wait(bar(B::kDQFree), it & 1, wc, kSiteBMmaDQ)) { ok = false; break; }
+                        // dV += P^T dO_{i+1} (P^T from the S^T columns)
+                        if (!mbar_wait_w(bar(B::kPFull), (it + 1) & 1, kSiteBMmaP)) { ok = false; break; }
                         tc_fence_after();
-                        qs = wait_q(it + 1);
-                        if (qs < 0) { ok = false; break; }
-                        mma_kk(tS, sK, sQ + qs * C::kTileBytes);
-                        mma_commit(bar(B::kSFull));
-                        dos = wait_do(it + 1);
-                        if (dos < 0) { ok = false; break; }
-                        mma_kk(tDP, sV, sDO + dos * C::kTileBytes);
-                        mma_commit(bar(B::kDPFull));
+                        const int dn = wait_do(it + 1);
+                        if (dn < 0) { ok = false; break; }
+                        mma_tn(tDV, tS, sDO + dn * C::kTileBytes, true);
+                        // dP^T_{i+1} once dQ_i has left the dP^T columns
+                        if (!mbar_wait_w(bar(B::kDQFree), it & 1, kSiteBMmaDQ)) { ok = false; break; }
+                        tc_fence_after();
+                        mma_kk(tDP, sV, sDO + dn * C::kTileBytes);
+                        umma_commit(bar(B::kDPFull));
+                        umma_commit(bar(B::kDOEmpty + dn));
+                        if (it + 2 < n_it) {  // S^T_{i+2}: P^T_{i+1} is read by dV_{i+1} first
+                            const int qn = wait_q(it + 2);
+                            if (qn < 0) { ok = false; break; }
+                            mma_kk(tS, sK, sQ + qn * C::kTileBytes);
+                            umma_commit(bar(B::kSFull));
+                        }
                     }
                 }
             } else {
                 for (int it = 0; ok && it < n_it; ++it) {
-                    if (!mbar_wait(bar(B::kPFull), it & 1, wc, kSiteBMmaP)) { ok = false; break; }
+                    if (!mbar_wait_w(bar(B::kPFull), it & 1, kSiteBMmaP)) { ok = false; break; }
                     tc_fence_after();
                     mma_tn(tDV, tS, sDO + dos * C::kTileBytes, it > 0);
-                    mma_commit(bar(B::kDOEmpty + dos));
+                    umma_commit(bar(B::kDOEmpty + dos));
                     int qs_next = -1;
                     if (it + 1 < n_it) {  // S^T_{i+1}: the S^T columns are free after dV_i
                         qs_next = wait_q(it + 1);
                         if (qs_next < 0) { ok = false; break; }
                         mma_kk(tS, sK, sQ + qs_next * C::kTileBytes);
-                        mma_commit(bar(B::kSFull));
+                        umma_commit(bar(B::kSFull));
                     }
-                    if (!mbar_wait(bar(B::kDSFull), it & 1, wc, kSiteBMmaDS)) { ok = false; break; }
+                    if (!mbar_wait_w(bar(B::kDSFull), it & 1, kSiteBMmaDS)) { ok = false; break; }
                     tc_fence_after();
                     mma_tn(tDK, tDP, sQ + qs * C::kTileBytes, it > 0);
-                    mma_commit(bar(B::kQEmpty + qs));
+                    umma_commit(bar(B::kQEmpty + qs));
                     qs = qs_next;
                     if (it + 1 < n_it) {  // dP^T_{i+1}: its columns are free after dK_i
                         dos = wait_do(it + 1);
                         if (dos < 0) { ok = false; break; }
                         mma_kk(tDP, sV, sDO + dos * C::kTileBytes);
-                        mma_commit(bar(B::kDPFull));
+                        umma_commit(bar(B::kDPFull));
                     }
                 }
             }
             // Drain the tensor pipe before tensor memory can be released; the dK/dV
             // epilogue waits on the same commit (it follows the last dK product).
-            mma_commit(bar(B::kDrain));
+            umma_commit(bar(B::kDrain));
             mbar_wait_drain(bar(B::kDrain), 0, wc, kSiteBDrain);
         }
     } else if (warp < 4) {
@@ -444,9 +489,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int i = q_block(it);
-            const int qs = it % C::kQStages;
+            const int vs = it % C::kVecStages;
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kSFull), it & 1, wc, kSiteBSoftS) &&
-                                             mbar_wait(bar(B::kQFull + qs), (it / C::kQStages) & 1, wc, kSiteBSoftL));
+                                             mbar_wait(bar(B::kVecFull + vs), (it / C::kVecStages) & 1, wc, kSiteBSoftL));
             if (!ok) break;
             tc_fence_after();
             // P^T = 2^(S^T * scale*log2e - L2) in fp32, kept as packed bf16: the same values
@@ -455,7 +500,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             {
                 uint32_t sr[128];
                 tmem_ld_x128(tSr, sr);
-                const float2 *nL = reinterpret_cast<const float2 *>(Lvec + qs * kTileRows);  // -L * log2 e
+                const float2 *nL = reinterpret_cast<const float2 *>(Lvec + vs * kTileRows);  // -L * log2 e
                 const float2 sl2 = make_float2(scale_log2, scale_log2);
                 // causal: query q sees key c iff c <= q (same block offsets on the diagonal)
                 const int qmin = (causal && i == j) ? c : 0;
@@ -483,7 +528,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDPFull), it & 1, wc, kSiteBSoftDP));
             if (!ok) break;
             tc_fence_after();
-            const float2 *D2 = reinterpret_cast<const float2 *>(Dvec + qs * kTileRows);
+            const float2 *D2 = reinterpret_cast<const float2 *>(Dvec + vs * kTileRows);
             // 32 query columns at a time; the load of the next chunk is in flight while
             // this chunk is computed and stored
             uint32_t rbuf[2][32];
@@ -556,7 +601,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;                   // query row within the block
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tDQr = tmem + lane_off + C::kSCol;   // dQ_i accumulates in the S^T columns
+        const uint32_t tDQr = tmem + lane_off + C::kDPCol;  // dQ_i accumulates in the dP^T columns
         bool ok = true;
         for (int it = 0; kDQ && it < n_it; ++it) {
             const int i = q_block(it);
@@ -808,7 +853,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this loop (every wait is warp-uniform) and lane 0 issues.
+        {
+            auto mbar_wait_w = [&](uint32_t b, uint32_t parity, int site) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
+            };
             const uint32_t tSD[2] = {tmem, tmem + 128u};
             const uint32_t tDQ[2] = {tmem + C::kDQCol, tmem + C::kDQCol + D};
             auto active = [&](int t, int j) { return j < ntile[t]; };
@@ -817,19 +866,19 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                 for (int kk = 0; kk < C::kKSteps; ++kk) {
                     const uint32_t off = (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32;
-                    mma_ss<false>(d_tmem, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(b_tile + off, 16, 1024),
+                    umma_ss(d_tmem, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(b_tile + off, 16, 1024),
                                   C::kIdescS, kk > 0 ? 1u : 0u);
                 }
             };
             auto wait_k = [&](int j) -> int {
                 const int s = j % C::kKStages;
-                if (!mbar_wait(bar(B::kKFull + s), (j / C::kKStages) & 1, wc, kSiteQMmaK)) return -1;
+                if (!mbar_wait_w(bar(B::kKFull + s), (j / C::kKStages) & 1, kSiteQMmaK)) return -1;
                 tc_fence_after();
                 return s;
             };
             auto wait_v = [&](int j) -> int {
                 const int s = j % C::kVStages;
-                if (!mbar_wait(bar(B::kVFull + s), (j / C::kVStages) & 1, wc, kSiteQMmaV)) return -1;
+                if (!mbar_wait_w(bar(B::kVFull + s), (j / C::kVStages) & 1, kSiteQMmaV)) return -1;
                 tc_fence_after();
                 return s;
             };
@@ -839,15 +888,15 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 if (vs < 0) return false;
                 for (int t = 0; t < 2; ++t) {
                     if (!active(t, j)) continue;
-                    if (!mbar_wait(bar(B::kSRead + t), j & 1, wc, kSiteQMmaS)) return false;
+                    if (!mbar_wait_w(bar(B::kSRead + t), j & 1, kSiteQMmaS)) return false;
                     tc_fence_after();
                     mma_rows(tSD[t], sDO + t * C::kTileBytes, sV + vs * C::kTileBytes);
-                    mma_commit(bar(B::kDPFull + t));
+                    umma_commit(bar(B::kDPFull + t));
                 }
-                mma_commit(bar(B::kVEmpty + vs));
+                umma_commit(bar(B::kVEmpty + vs));
                 return true;
             };
-            bool ok = nmax > 0 && mbar_wait(bar(B::kQ), 0, wc, kSiteQMmaQ);
+            bool ok = nmax > 0 && mbar_wait_w(bar(B::kQ), 0, kSiteQMmaQ);
             if (ok) {
                 tc_fence_after();
                 int ks = wait_k(0);
@@ -856,7 +905,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     for (int t = 0; t < 2; ++t) {
                         if (!active(t, 0)) continue;
                         mma_rows(tSD[t], sQ + t * C::kTileBytes, sK + ks * C::kTileBytes);
-                        mma_commit(bar(B::kSFull + t));
+                        umma_commit(bar(B::kSFull + t));
                     }
                     ok = issue_dp(0);
                 }
@@ -867,26 +916,26 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int t = 0; ok && t < 2; ++t) {
                     if (!active(t, j)) continue;
                     // dQ_t += dS_t K_j, then S_t for the next key block into the same columns
-                    if (!mbar_wait(bar(B::kDSFull + t), j & 1, wc, kSiteQMmaDS)) { ok = false; break; }
+                    if (!mbar_wait_w(bar(B::kDSFull + t), j & 1, kSiteQMmaDS)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < C::kRowSteps; ++kk)
-                        mma_ts<false>(tDQ[t], tSD[t] + kk * 8u,
+                        umma_ts(tDQ[t], tSD[t] + kk * 8u,
                                       sdesc_sw128(sK + ks * C::kTileBytes + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024),
                                       C::kIdescDQ, (j > 0 || kk > 0) ? 1u : 0u);
                     if (active(t, j + 1)) {
                         if (ks_next < 0) ks_next = wait_k(j + 1);
                         if (ks_next < 0) { ok = false; break; }
                         mma_rows(tSD[t], sQ + t * C::kTileBytes, sK + ks_next * C::kTileBytes);
-                        mma_commit(bar(B::kSFull + t));
+                        umma_commit(bar(B::kSFull + t));
                     }
                 }
                 if (!ok) break;
-                mma_commit(bar(B::kKEmpty + ks));
+                umma_commit(bar(B::kKEmpty + ks));
                 if (j + 1 < nmax) ok = issue_dp(j + 1);
             }
             // Both tiles' dQ are complete once everything issued so far has retired.
-            mma_commit(bar(B::kDone));
+            umma_commit(bar(B::kDone));
             mbar_wait_drain(bar(B::kDone), 0, wc, kSiteQDrain);
         }
     } else {
@@ -1011,7 +1060,6 @@ int grid_for(long long work_items, int per_block) {
 
 template <int D>
 cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
-    using C = BwdCfg<D>;
     const long long rows = static_cast<long long>(a.BH) * a.Npad;
     bwd_pre_kernel<D><<<grid_for(rows, 64), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(a.o), static_cast<const __nv_bfloat16 *>(a.dout), a.lse, a.delta,
@@ -1020,13 +1068,14 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
 
     auto kern = a.deterministic ? bwd_main_kernel<D, false> : bwd_main_kernel<D, true>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    const int smem_bytes = a.deterministic ? BwdCfg<D, false>::kSmemBytes : BwdCfg<D, true>::kSmemBytes;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     const int nkv = a.Npad / kTileRows;
     const long long blocks = static_cast<long long>(a.BH / a.group) * nkv;
     if (blocks <= 0 || blocks > INT_MAX) return cudaErrorInvalidValue;
     const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-    kern<<<static_cast<unsigned>(blocks), kThreads, C::kSmemBytes, stream>>>(
+    kern<<<static_cast<unsigned>(blocks), kThreads, smem_bytes, stream>>>(
         a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.lse2, a.delta, static_cast<__nv_bfloat16 *>(a.dk),
         static_cast<__nv_bfloat16 *>(a.dv), a.N, a.Npad, nkv, a.group, a.scale, scale_log2, a.causal, a.status);
     e = cudaGetLastError();

@@ -270,12 +270,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this loop (every wait is warp-uniform) and lane 0 issues.
+        {
+            auto mbar_wait_w = [&](uint32_t b, uint32_t parity, int site) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
+            };
             const uint32_t tS[2] = {tmem, tmem + 128u};
             const uint32_t tO[2] = {tmem + C::kOCol, tmem + C::kOCol + D};
             auto wait_kv = [&](int seq) -> int {
                 const int s = seq % C::kStages;
-                if (!mbar_wait(bar(B::kKVFull + s), (seq / C::kStages) & 1, wc, kSiteMmaKV)) return -1;
+                if (!mbar_wait_w(bar(B::kKVFull + s), (seq / C::kStages) & 1, kSiteMmaKV)) return -1;
                 tc_fence_after();
                 return s;
             };
@@ -285,7 +289,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     const uint32_t off = (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32;
                     const uint64_t a = sdesc_sw128(sQ + t * C::kTileBytes + off, 16, 1024);
                     const uint64_t b = sdesc_sw128(sKV + s * C::kTileBytes + off, 16, 1024);
-                    mma_ss<C::kTF32>(tS[t], a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    umma_ss<C::kTF32>(tS[t], a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int s, bool acc) {
@@ -296,10 +300,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                         C::kTF32 ? sdesc_sw128(base + C::kVtOff + (kk >> 2) * C::kVtBoxBytes + (kk & 3) * 32, 16, 1024)
                                  : sdesc_sw128(sKV + s * C::kTileBytes + kk * C::kKStep * kBoxBytes,
                                                C::kBoxTileBytes, 1024);
-                    mma_ts<C::kTF32>(tO[t], tS[t] + kk * 8u, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                    umma_ts<C::kTF32>(tO[t], tS[t] + kk * 8u, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = mbar_wait(bar(B::kQ), 0, wc, kSiteMmaQ);
+            bool ok = mbar_wait_w(bar(B::kQ), 0, kSiteMmaQ);
             if (ok) {
                 const int sk = wait_kv(0);
                 ok = sk >= 0;
@@ -307,16 +311,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     for (int t = 0; t < 2; ++t) {
                         if (ntile[t] == 0) continue;
                         issue_qk(t, sk);
-                        mma_commit(bar(B::kSFull + t));
+                        umma_commit(bar(B::kSFull + t));
                     }
-                    mma_commit(bar(B::kKVEmpty + sk));
+                    umma_commit(bar(B::kKVEmpty + sk));
                 }
             }
             for (int j = 0; ok && j < nmax; ++j) {
                 int sv;
                 if constexpr (C::kTF32) {
                     // V^T of V_j written by the producer warp (V tiles always use stage 1)
-                    sv = mbar_wait(bar(B::kVtFull), j & 1, wc, kSiteMmaKV) ? 1 : -1;
+                    sv = mbar_wait_w(bar(B::kVtFull), j & 1, kSiteMmaKV) ? 1 : -1;
                     tc_fence_after();
                 } else {
                     sv = wait_kv(2 * j + 1);
@@ -325,25 +329,25 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 int skn = -1;
                 for (int t = 0; t < 2; ++t) {
                     if (j >= ntile[t]) continue;
-                    if (!mbar_wait(bar(B::kPFull + t), j & 1, wc, kSiteMmaP)) { ok = false; break; }
+                    if (!mbar_wait_w(bar(B::kPFull + t), j & 1, kSiteMmaP)) { ok = false; break; }
                     tc_fence_after();
                     issue_pv(t, sv, j > 0);
-                    mma_commit(bar(B::kODone + t));
+                    umma_commit(bar(B::kODone + t));
                     if (j + 1 < ntile[t]) {
                         if (skn < 0) {
                             skn = wait_kv(2 * (j + 1));
                             if (skn < 0) { ok = false; break; }
                         }
                         issue_qk(t, skn);
-                        mma_commit(bar(B::kSFull + t));
+                        umma_commit(bar(B::kSFull + t));
                     }
                 }
                 if (!ok) break;
-                mma_commit(bar(B::kKVEmpty + sv));
-                if (skn >= 0) mma_commit(bar(B::kKVEmpty + skn));
+                umma_commit(bar(B::kKVEmpty + sv));
+                if (skn >= 0) umma_commit(bar(B::kKVEmpty + skn));
             }
             // Drain the tensor pipe before tensor memory can be released.
-            mma_commit(bar(B::kMmaDone));
+            umma_commit(bar(B::kMmaDone));
             mbar_wait_drain(bar(B::kMmaDone), 0, wc, kSiteMmaDrain);
         }
     } else {
