@@ -42,8 +42,8 @@ REF_STEP_ROWS = 32      # query rows per head per step of the reference arm
 # they had when the counters were taken; after any change it reads as null until the
 # capture is repeated.
 TRAFFIC = {
-    "bwd": (1985.6e6, ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"), "450695c0097d4576"),
-    "fwd": (495.4e6, ("fa_fwd.cu", "ptx.cuh", "fa_internal.h"), "112083cc9a0bc3e9"),
+    "bwd": (1990.0e6, ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"), "f9a282d30e4c60c6"),
+    "fwd": (495.3e6, ("fa_fwd.cu", "ptx.cuh", "fa_internal.h"), "91a1e5ef35fb287e"),
 }
 
 
