@@ -205,10 +205,11 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_dict(w, shape=None):
+def config_dict(w, shape=None, deterministic=False):
     B, H, N, d = shape if shape else (w.B, w.H, w.N, w.d)
     return {"workload": f"fwd+bwd causal bf16 B={B} H={H} N={N} d={d}",
             "B": B, "H": H, "N": N, "d": d, "causal": CAUSAL, "scale": "1/sqrt(d)",
+            "backward": "deterministic (fa_bwd_deterministic)" if deterministic else "default (fa_bwd)",
             "inputs": "iid N(0,1) rounded to bf16, seeds 3001-3004",
             "l2": "inputs 512 MiB > L2; L2 flushed (256 MiB write) between timed steps",
             "parallelism": "one independent replica per GPU"}
@@ -233,13 +234,16 @@ def run_ours(args, world, rank, local):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(fa.bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    det = bool(args.deterministic)
+    ws_bytes = (fa.bwd_deterministic_workspace_size if det else fa.bwd_workspace_size)(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         fa.fwd(q, k, v, causal=CAUSAL, scale=scale, out=o, lse=lse)
-        fa.bwd(q, k, v, o, lse, do, causal=CAUSAL, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+        fa.bwd(q, k, v, o, lse, do, causal=CAUSAL, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+               deterministic=det)
 
     for _ in range(args.warmup):
         step()
@@ -261,7 +265,8 @@ def run_ours(args, world, rank, local):
             ev[i][0].record(stream)
             fa.fwd(q, k, v, causal=CAUSAL, scale=scale, out=o, lse=lse)
             ev[i][1].record(stream)
-            fa.bwd(q, k, v, o, lse, do, causal=CAUSAL, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+            fa.bwd(q, k, v, o, lse, do, causal=CAUSAL, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                   deterministic=det)
             ev[i][2].record(stream)
         torch.cuda.synchronize(dev)
     if world > 1:
@@ -289,13 +294,15 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(w, args.shape),
+        "config": config_dict(w, args.shape, det),
         "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
         "fwd_ms": statistics.mean(t_fwd), "bwd_ms": statistics.mean(t_bwd),
         "fwd_frac_of_peak": fwd_tf / peak_burst, "bwd_frac_of_peak": bwd_tf / peak_burst,
         "roofline": {"bound": "tensor", "kernel": f"{dominant} (CUDA events around the C-ABI call)",
                      "achieved": dom_tf, "peak": peak_burst, "unit": "TFLOP/s",
-                     "frac": dom_tf / peak_burst, "traffic": measured_traffic(dominant, args.shape),
+                     "frac": dom_tf / peak_burst,
+                     "traffic": measured_traffic(dominant + ("_det" if det and dominant == "bwd" else ""),
+                                                 args.shape),
                      "traffic_unit": "bytes per call (DRAM read + write, ncu)",
                      "peak_source": f"{peak_src} bf16 burst"},
         "e2e": e2e,
@@ -358,6 +365,8 @@ def main():
                     help="skip timing the fp64 oracle on the host")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time the deterministic backward (fa_bwd_deterministic) in the step")
     ap.add_argument("--shape", type=lambda x: tuple(int(v) for v in x.split(",")), default=None,
                     metavar="B,H,N,d",
                     help="run another shape (profiling captures on a smaller case); the metric "
