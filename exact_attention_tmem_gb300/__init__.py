@@ -16,8 +16,8 @@ import torch
 from . import _lib
 from ._lib import FaError  # noqa: F401
 
-__all__ = ["fwd", "bwd", "bwd_workspace_size", "bwd_deterministic_workspace_size", "device_status", "build",
-           "FaError"]
+__all__ = ["fwd", "bwd", "decode", "bwd_workspace_size", "bwd_deterministic_workspace_size",
+           "decode_workspace_size", "device_status", "build", "FaError"]
 
 
 def build(force: bool = False) -> str:
@@ -138,6 +138,37 @@ def bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
         st, name = lib.fa_bwd_gqa(*args, B, H, Hkv, N, d, scale, int(bool(causal)), stream), "fa_bwd_gqa"
     _lib.check(st, name)
     return dq, dk, dv
+
+
+def decode_workspace_size(B: int, H: int, Hkv: int, Nk: int, d: int) -> int:
+    return int(_lib.load().fa_decode_workspace_size(B, H, Hkv, Nk, d))
+
+
+def decode(q, k, v, scale: float | None = None, out=None, lse=None, workspace=None, num_chunks: int = 0):
+    """One query row per head against all keys: q [B, H, d], k and v [B, Hkv, Nk, d]
+    (bf16, Hkv dividing H, H / Hkv <= 8).  Returns (o [B, H, d] bf16, lse [B, H] fp32).
+    The keys are split into chunks merged on the device (num_chunks = 0: automatic)."""
+    if q.dim() != 3 or k.dim() != 4:
+        raise ValueError("expected q [B, H, d] and k, v [B, Hkv, Nk, d]")
+    B, H, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if k.shape[0] != B or k.shape[3] != d or H % Hkv != 0:
+        raise ValueError("q and k/v must agree in B and d, and Hkv must divide H")
+    _check_tensors(torch.bfloat16, q.shape, q)
+    _check_tensors(torch.bfloat16, k.shape, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensors(torch.bfloat16, q.shape, q, out)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H] tensor")
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_size(B, H, Hkv, Nk, d), dtype=torch.uint8, device=q.device)
+    st = _lib.load().fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                               B, H, Hkv, Nk, d, scale, int(num_chunks), _stream_ptr(q.device))
+    _lib.check(st, "fa_decode")
+    return out, lse
 
 
 def device_status(stream=None) -> int:

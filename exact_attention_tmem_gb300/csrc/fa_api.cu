@@ -64,6 +64,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
     bool ready = false;
     bool supported = false;
+    int sm_count = 0;
     unsigned int *status = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
@@ -83,6 +84,8 @@ int device_state(DeviceState **out) {
         e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (e != cudaSuccess) return cuda_fail(e);
         s.supported = (major == 10 && minor == 3);
+        e = cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
         if (s.supported) {
             void *p = nullptr;
             e = cudaGetSymbolAddress(&p, g_status_word);
@@ -292,6 +295,89 @@ extern "C" int fa_bwd_deterministic(const void *q, const void *k, const void *v,
                                     int causal, fa_stream_t stream) {
     return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal,
                       true, stream);
+}
+
+namespace fa {
+namespace {
+// Decoding: key chunks are whole 64-key stages; at most kDecodeMaxChunks per head.
+constexpr int kDecodeChunkAlign = 64;
+constexpr int kDecodeMaxChunks = 256;
+
+int decode_max_chunks(int Nk) {
+    const int stages = (Nk + kDecodeChunkAlign - 1) / kDecodeChunkAlign;
+    return stages < kDecodeMaxChunks ? stages : kDecodeMaxChunks;
+}
+
+int check_decode(int B, int H, int Hkv, int Nk, int d) {
+    int st = check_shape(B, H, Nk, d, Hkv);
+    if (st != FA_OK) return st;
+    if (H / Hkv > 8) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+size_t decode_workspace(int B, int H, int Nk, int d) {
+    const size_t slots = static_cast<size_t>(B) * H * decode_max_chunks(Nk);
+    const size_t vec = (slots * sizeof(float) + 255) / 256 * 256;
+    return 2 * vec + slots * d * sizeof(float);
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nk, int d) {
+    if (check_decode(B, H, Hkv, Nk, d) != FA_OK) return 0;
+    return decode_workspace(B, H, Nk, d);
+}
+
+extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, void *workspace,
+                         size_t workspace_bytes, int B, int H, int Hkv, int Nk, int d, float scale,
+                         int num_chunks, fa_stream_t stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    int st = check_decode(B, H, Hkv, Nk, d);
+    if (st != FA_OK) return st;
+    if (!std::isfinite(scale) || num_chunks < 0) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse))
+        return FA_ERR_ALIGNMENT;
+    if (workspace == nullptr || workspace_bytes < decode_workspace(B, H, Nk, d)) return FA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGNMENT;
+    DeviceState *ds = nullptr;
+    st = device_state(&ds);
+    if (st != FA_OK) return st;
+    const int max_chunks = decode_max_chunks(Nk);
+    const int BHkv = B * Hkv;
+    int want = num_chunks;
+    if (want == 0) {  // enough CTAs for two per SM
+        const long long target = 2LL * (ds->sm_count > 0 ? ds->sm_count : 1);
+        want = static_cast<int>((target + BHkv - 1) / BHkv);
+    }
+    if (want < 1) want = 1;
+    if (want > max_chunks) want = max_chunks;
+    const int stages = (Nk + kDecodeChunkAlign - 1) / kDecodeChunkAlign;
+    const int chunk_stages = (stages + want - 1) / want;
+    DecodeArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    const size_t slots = static_cast<size_t>(B) * H * max_chunks;
+    const size_t vec = (slots * sizeof(float) + 255) / 256 * 256;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.part_m = reinterpret_cast<float *>(ws);
+    a.part_l = reinterpret_cast<float *>(ws + vec);
+    a.part_acc = reinterpret_cast<float *>(ws + 2 * vec);
+    a.BHkv = BHkv;
+    a.group = H / Hkv;
+    a.Nk = Nk;
+    a.d = d;
+    a.chunk_keys = chunk_stages * kDecodeChunkAlign;
+    a.num_chunks = (Nk + a.chunk_keys - 1) / a.chunk_keys;
+    a.max_chunks = max_chunks;
+    a.scale = scale;
+    a.status = ds->status;
+    cudaError_t e = launch_decode_bf16(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
 }
 
 extern "C" int fa_get_device_status(fa_stream_t stream) {

@@ -39,10 +39,25 @@ struct BwdArgs {
     unsigned int *status;
 };
 
-// Kernel launchers (fa_fwd.cu, fa_bwd.cu).  They return the launch's cudaError_t.
+// Decoding: one query row per head ([B*H, d]) against K, V [B*Hkv, Nk, d]; the keys of
+// each key/value head are split into num_chunks chunks of chunk_keys keys (a multiple
+// of 64), whose partial (m, l, acc) triples land in the workspace before the merge.
+struct DecodeArgs {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    float *part_m, *part_l, *part_acc;   // workspace: [B*H, max_chunks] (+ [.., d] for acc)
+    int BHkv, group, Nk, d;
+    int chunk_keys, num_chunks, max_chunks;
+    float scale;
+    unsigned int *status;
+};
+
+// Kernel launchers (fa_fwd.cu, fa_bwd.cu, fa_decode.cu).  They return the launch's cudaError_t.
 cudaError_t launch_fwd_bf16(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd_bf16(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t stream);
 
 // Tile geometry shared by host and device code.
 constexpr int kTileRows = 128;     // rows of Q, K, V per tile

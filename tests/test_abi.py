@@ -208,3 +208,50 @@ def test_deterministic_valid_call_without_gpu_reports_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert bwd_det(lib) == _lib.FA_ERR_CUDA
+
+
+def dec(lib, ptrs=None, ws=W, ws_bytes=None, B=1, H=4, Hkv=2, Nk=1000, d=128, scale=0.1, chunks=0):
+    p = [A] * 5 if ptrs is None else ptrs
+    if ws_bytes is None:
+        ws_bytes = lib.fa_decode_workspace_size(B, H, Hkv, Nk, d) or (1 << 20)
+    return lib.fa_decode(*p, ws, ws_bytes, B, H, Hkv, Nk, d, ctypes.c_float(scale), chunks, None)
+
+
+def test_decode_workspace_size(lib):
+    B, H, Nk, d = 2, 8, 1000, 128           # 16 stages of 64 keys -> 16 chunk slots
+    slots = B * H * 16
+    vec = -(-(slots * 4) // 256) * 256
+    assert lib.fa_decode_workspace_size(B, H, 2, Nk, d) == 2 * vec + slots * d * 4
+    big = lib.fa_decode_workspace_size(1, 1, 1, 1 << 20, 64)   # capped at 256 chunks
+    assert big == 2 * 1024 + 256 * 64 * 4
+    assert lib.fa_decode_workspace_size(1, 4, 3, 100, 128) == 0      # Hkv does not divide H
+    assert lib.fa_decode_workspace_size(1, 18, 2, 100, 128) == 0     # group of 9
+    assert lib.fa_decode_workspace_size(1, 4, 2, 100, 96) == 0
+
+
+@pytest.mark.parametrize("which", range(5))
+def test_decode_null_pointer(lib, which):
+    ptrs = [A] * 5
+    ptrs[which] = None
+    assert dec(lib, ptrs) == _lib.FA_ERR_INVALID_ARG
+
+
+def test_decode_host_checks(lib):
+    assert dec(lib, ws=None) == _lib.FA_ERR_WORKSPACE
+    need = lib.fa_decode_workspace_size(1, 4, 2, 1000, 128)
+    assert dec(lib, ws_bytes=need - 1) == _lib.FA_ERR_WORKSPACE
+    assert dec(lib, ws=W + 64) == _lib.FA_ERR_ALIGNMENT
+    assert dec(lib, ptrs=[A, A, A + 8, A, A]) == _lib.FA_ERR_ALIGNMENT
+    assert dec(lib, Hkv=3) == _lib.FA_ERR_INVALID_ARG
+    assert dec(lib, H=18, Hkv=2) == _lib.FA_ERR_UNSUPPORTED
+    assert dec(lib, d=96) == _lib.FA_ERR_UNSUPPORTED
+    assert dec(lib, Nk=0) == _lib.FA_ERR_INVALID_ARG
+    assert dec(lib, scale=float("nan")) == _lib.FA_ERR_INVALID_ARG
+    assert dec(lib, chunks=-1) == _lib.FA_ERR_INVALID_ARG
+
+
+def test_decode_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert dec(lib) == _lib.FA_ERR_CUDA
