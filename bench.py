@@ -205,6 +205,112 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+DECODE_METRIC = "decode K/V read bandwidth, bf16, one query row per head (fa_decode)"
+DECODE_SHAPE = (8, 32, 32, 32768, 128)     # B, H, Hkv, Nk, d
+
+
+def run_decode(args, world, rank, local):
+    """Decoding: one query row per head against Nk keys (split-key kernel + merge).
+    The metric is the compulsory K/V (+ q, o) bytes per call over the call's time,
+    against the measured HBM copy bandwidth: the kernel streams K and V once."""
+    import torch
+    import exact_attention_tmem_gb300 as fa
+    from exact_attention_tmem_gb300 import inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.build()
+    B, H, Hkv, Nk, d = args.decode_shape or DECODE_SHAPE
+    scale = 1.0 / math.sqrt(d)
+    q_h = inputs.normal((B, H, d), 21001)
+    k_h = inputs.normal((B, Hkv, Nk, d), 21002)
+    v_h = inputs.normal((B, Hkv, Nk, d), 21003)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.decode_workspace_size(B, H, Hkv, Nk, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nbytes = 2 * B * Hkv * Nk * d * 2 + 2 * B * H * d * 2 + B * H * 4
+
+    def call():
+        fa.decode(q, k, v, scale=scale, out=o, lse=lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        call()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    status = fa.device_status()
+    t = [e[0].elapsed_time(e[1]) for e in ev]
+    total_ms = max_over_ranks(sum(t), dev)
+    gbs = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
+    # end to end: the query rows come from pinned host memory, o and lse go back; the
+    # K/V cache stays resident on the device as a decoder's cache would
+    e2e = None
+    if not args.no_e2e:
+        hq = q_h.pin_memory()
+        ho = torch.empty_like(q_h).pin_memory()
+        hl = torch.empty((B, H), dtype=torch.float32).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            q.copy_(hq, non_blocking=True)
+            call()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / args.steps
+        e2e = {"value": world * nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": hq.numel() * 2, "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4,
+               "ms_per_step": ms}
+    if rank != 0:
+        return
+    _, _, hbm, peak_src = peaks()
+    line = {
+        "metric": DECODE_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"decode B={B} H={H} Hkv={Hkv} Nk={Nk} d={d}", "B": B, "H": H, "Hkv": Hkv,
+                   "Nk": Nk, "d": d, "scale": "1/sqrt(d)", "inputs": "iid N(0,1) rounded to bf16, seeds 21001-21003",
+                   "l2": "K/V larger than L2; L2 flushed (256 MiB write) between timed calls",
+                   "parallelism": "one independent replica per GPU"},
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel + decode_combine_kernel (CUDA events around "
+                     "the C-ABI call)", "achieved": gbs / world, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / world / hbm, "traffic": None,
+                     "algorithmic_bytes_per_call": nbytes, "peak_source": f"{peak_src} HBM copy"},
+        "e2e": e2e, "gpu_launches": 2 * args.steps, "device_status": status, "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        from oracle import decode as odec
+        heads = min(B * H, 4)
+        f = inputs.as_f64
+        qs, ks, vs = f(q_h[0, :heads])[None], f(k_h[0]), f(v_h[0])
+        kv = [h // (H // Hkv) for h in range(heads)]
+        t0 = time.perf_counter()
+        for h in range(heads):
+            odec.attention_decode(qs[:, h:h + 1], ks[None, kv[h]:kv[h] + 1], vs[None, kv[h]:kv[h] + 1], scale)
+        dt = time.perf_counter() - t0
+        sample_bytes = heads * 2 * Nk * d * 2
+        line["cpu_baseline"] = {"value": sample_bytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{heads} query heads of batch 0 (numpy fp64), {dt:.2f} s"}
+    print(json.dumps(line), flush=True)
+
+
 def config_dict(w, shape=None, deterministic=False):
     B, H, N, d = shape if shape else (w.B, w.H, w.N, w.d)
     return {"workload": f"fwd+bwd causal bf16 B={B} H={H} N={N} d={d}",
@@ -365,6 +471,10 @@ def main():
                     help="skip timing the fp64 oracle on the host")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the decoding kernel (one query row per head) instead of the fwd+bwd step")
+    ap.add_argument("--decode-shape", type=lambda x: tuple(int(v) for v in x.split(",")), default=None,
+                    metavar="B,H,Hkv,Nk,d", help="decode workload (default 8,32,32,32768,128)")
     ap.add_argument("--deterministic", action="store_true",
                     help="time the deterministic backward (fa_bwd_deterministic) in the step")
     ap.add_argument("--shape", type=lambda x: tuple(int(v) for v in x.split(",")), default=None,
@@ -379,7 +489,10 @@ def main():
         run_reference(args, world, rank)
     else:
         world, rank, local = dist_setup("nccl")
-        run_ours(args, world, rank, local)
+        if args.decode:
+            run_decode(args, world, rank, local)
+        else:
+            run_ours(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
