@@ -965,6 +965,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             {
                 uint32_t sr[128];
                 tmem_ld_x128(tSDr, sr);
+                // S is in registers: dP may overwrite its columns while P is computed
+                tc_fence_before();
+                mbar_arrive(bar(B::kSRead + t));
                 // keys past N, and (causal) keys after this query, get probability 0
                 const int kmax = min(N - 1 - j * kTileRows, causal ? q - j * kTileRows : kTileRows - 1);
                 if (kmax >= kTileRows - 1) {
@@ -983,8 +986,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(bar(B::kSRead + t));
             // dS = P o (dP - D), packed bf16 over the first 64 columns
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDPFull + t), j & 1, wc, kSiteQSoftDP));
             if (!ok) break;
