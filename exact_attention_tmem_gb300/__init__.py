@@ -16,8 +16,8 @@ import torch
 from . import _lib
 from ._lib import FaError  # noqa: F401
 
-__all__ = ["fwd", "bwd", "decode", "bwd_workspace_size", "bwd_deterministic_workspace_size",
-           "decode_workspace_size", "device_status", "build", "FaError"]
+__all__ = ["fwd", "bwd", "decode", "quantize_qk_fp8", "quantize_v_fp8", "fwd_fp8", "bwd_workspace_size",
+           "bwd_deterministic_workspace_size", "decode_workspace_size", "device_status", "build", "FaError"]
 
 
 def build(force: bool = False) -> str:
@@ -168,6 +168,65 @@ def decode(q, k, v, scale: float | None = None, out=None, lse=None, workspace=No
                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                B, H, Hkv, Nk, d, scale, int(num_chunks), _stream_ptr(q.device))
     _lib.check(st, "fa_decode")
+    return out, lse
+
+
+def quantize_qk_fp8(x, signs=None):
+    """e4m3 codes of Q or K [B, H, N, d] (bf16) with one scale per (batch, head).  With
+    ``signs`` (a float32 tensor of +-1 of length d, the same for Q and K) every row is
+    first rotated by diag(signs) H / sqrt(d) (incoherent processing).  Returns
+    (codes as a uint8 tensor [B, H, N, d], descale float32 [B, H])."""
+    if x.dim() != 4:
+        raise ValueError("expected a [B, H, N, d] tensor")
+    B, H, N, d = x.shape
+    _check_tensors(torch.bfloat16, x.shape, x)
+    if signs is not None:
+        if signs.dtype != torch.float32 or tuple(signs.shape) != (d,) or not signs.is_cuda:
+            raise ValueError("signs must be a float32 CUDA tensor of length d")
+    x8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    descale = torch.empty((B, H), dtype=torch.float32, device=x.device)
+    st = _lib.load().fa_quantize_qk_fp8(x.data_ptr(), signs.data_ptr() if signs is not None else None,
+                                        x8.data_ptr(), descale.data_ptr(), B, H, N, d, _stream_ptr(x.device))
+    _lib.check(st, "fa_quantize_qk_fp8")
+    return x8, descale
+
+
+def quantize_v_fp8(v):
+    """e4m3 codes of V [B, H, N, d] (bf16), transposed to [B, H, d, Npad] (keys contiguous,
+    N padded to a multiple of 16 with zero codes), and descale float32 [B, H]."""
+    if v.dim() != 4:
+        raise ValueError("expected a [B, H, N, d] tensor")
+    B, H, N, d = v.shape
+    _check_tensors(torch.bfloat16, v.shape, v)
+    npad = (N + 15) // 16 * 16
+    vt8 = torch.empty((B, H, d, npad), dtype=torch.uint8, device=v.device)
+    descale = torch.empty((B, H), dtype=torch.float32, device=v.device)
+    st = _lib.load().fa_quantize_v_fp8(v.data_ptr(), vt8.data_ptr(), descale.data_ptr(), B, H, N, d,
+                                       _stream_ptr(v.device))
+    _lib.check(st, "fa_quantize_v_fp8")
+    return vt8, descale
+
+
+def fwd_fp8(q8, k8, vt8, descale_q, descale_k, descale_v, causal: bool = False, scale: float | None = None,
+            out=None, lse=None):
+    """Forward pass on e4m3 codes (from quantize_qk_fp8 / quantize_v_fp8; d = 128):
+    returns (o bf16 [B, H, N, d], lse float32 [B, H, N])."""
+    B, H, N, d = q8.shape
+    Hkv = k8.shape[1]
+    if q8.dtype != torch.uint8 or k8.dtype != torch.uint8 or vt8.dtype != torch.uint8:
+        raise ValueError("q8, k8 and vt8 must be uint8 code tensors")
+    if tuple(k8.shape) != (B, Hkv, N, d) or tuple(vt8.shape) != (B, Hkv, d, (N + 15) // 16 * 16):
+        raise ValueError("k8 must be [B, Hkv, N, d] and vt8 [B, Hkv, d, Npad]")
+    for t in (q8, k8, vt8, descale_q, descale_k, descale_v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    st = _lib.load().fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), descale_q.data_ptr(),
+                                descale_k.data_ptr(), descale_v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                B, H, Hkv, N, d, scale, int(bool(causal)), _stream_ptr(q8.device))
+    _lib.check(st, "fa_fwd_fp8")
     return out, lse
 
 

@@ -25,6 +25,7 @@ FA_ERR_DEVICE_TIMEOUT = 6
 EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_gqa",
             "fa_bwd_deterministic_workspace_size", "fa_bwd_deterministic", "fa_bwd_noalloc",
             "fa_decode_workspace_size", "fa_decode",
+            "fa_fp8_v_bytes", "fa_quantize_qk_fp8", "fa_quantize_v_fp8", "fa_fwd_fp8",
             "fa_get_device_status", "fa_selftest_wait_timeout", "fa_status_string",
             "fa_last_cuda_error")
 NOALLOC_SCRATCH_BYTES = 64 << 20   # FA_NOALLOC_SCRATCH_BYTES in include/fa.h
@@ -71,6 +72,14 @@ def load() -> ctypes.CDLL:
         lib.fa_decode_workspace_size.restype = Z
         lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, vp, Z, I, I, I, I, I, F, I, vp]
         lib.fa_decode.restype = I
+        lib.fa_fp8_v_bytes.argtypes = [I, I, I, I]
+        lib.fa_fp8_v_bytes.restype = Z
+        lib.fa_quantize_qk_fp8.argtypes = [vp, vp, vp, vp, I, I, I, I, vp]
+        lib.fa_quantize_qk_fp8.restype = I
+        lib.fa_quantize_v_fp8.argtypes = [vp, vp, vp, I, I, I, I, vp]
+        lib.fa_quantize_v_fp8.restype = I
+        lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, F, I, vp]
+        lib.fa_fwd_fp8.restype = I
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, vp]
         lib.fa_bwd_noalloc.restype = I
         lib.fa_get_device_status.argtypes = [vp]

@@ -380,6 +380,86 @@ extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, f
     return FA_OK;
 }
 
+// ---- FP8 forward and its quantization ----
+namespace fa {
+namespace {
+size_t fp8_npad(int N) { return (static_cast<size_t>(N) + 15) / 16 * 16; }
+}  // namespace
+}  // namespace fa
+
+extern "C" size_t fa_fp8_v_bytes(int B, int H, int N, int d) {
+    if (check_shape(B, H, N, d, H) != FA_OK) return 0;
+    return static_cast<size_t>(B) * H * d * fp8_npad(N);
+}
+
+extern "C" int fa_quantize_qk_fp8(const void *x, const float *signs, void *x8, float *descale, int B, int H, int N,
+                                  int d, fa_stream_t stream) {
+    if (!x || !x8 || !descale) return FA_ERR_INVALID_ARG;
+    int st = check_shape(B, H, N, d, H);
+    if (st != FA_OK) return st;
+    if (!aligned16(x) || !aligned16(x8) || !aligned4(descale) || (signs && !aligned4(signs))) return FA_ERR_ALIGNMENT;
+    DeviceState *ds = nullptr;
+    st = device_state(&ds);
+    if (st != FA_OK) return st;
+    cudaError_t e = launch_quantize_qk_fp8(x, signs, x8, descale, B * H, N, d, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
+extern "C" int fa_quantize_v_fp8(const void *v, void *vt8, float *descale, int B, int H, int N, int d,
+                                 fa_stream_t stream) {
+    if (!v || !vt8 || !descale) return FA_ERR_INVALID_ARG;
+    int st = check_shape(B, H, N, d, H);
+    if (st != FA_OK) return st;
+    if (!aligned16(v) || !aligned16(vt8) || !aligned4(descale)) return FA_ERR_ALIGNMENT;
+    DeviceState *ds = nullptr;
+    st = device_state(&ds);
+    if (st != FA_OK) return st;
+    cudaError_t e = launch_quantize_v_fp8(v, vt8, descale, B * H, N, static_cast<int>(fp8_npad(N)), d,
+                                          reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
+extern "C" int fa_fwd_fp8(const void *q8, const void *k8, const void *vt8, const float *descale_q,
+                          const float *descale_k, const float *descale_v, void *o, float *lse, int B, int H, int Hkv,
+                          int N, int d, float scale, int causal, fa_stream_t stream) {
+    if (!q8 || !k8 || !vt8 || !descale_q || !descale_k || !descale_v || !o || !lse) return FA_ERR_INVALID_ARG;
+    int st = check_shape(B, H, N, d, Hkv);
+    if (st != FA_OK) return st;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) || !aligned4(lse) ||
+        !aligned4(descale_q) || !aligned4(descale_k) || !aligned4(descale_v))
+        return FA_ERR_ALIGNMENT;
+    DeviceState *ds = nullptr;
+    st = device_state(&ds);
+    if (st != FA_OK) return st;
+    Fp8FwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const int BH = B * H, BHkv = B * Hkv;
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if ((st = make_tmap(&a.tm_q, q8, u8, 1, d, N, BH)) != FA_OK) return st;
+    if ((st = make_tmap(&a.tm_k, k8, u8, 1, d, N, BHkv)) != FA_OK) return st;
+    // V codes [BHkv, d, Npad]: keys innermost, a box is 128 keys of 128 rows
+    if ((st = make_tmap(&a.tm_vt, vt8, u8, 1, static_cast<int>(fp8_npad(N)), d, BHkv)) != FA_OK) return st;
+    a.dsc_q = descale_q;
+    a.dsc_k = descale_k;
+    a.dsc_v = descale_v;
+    a.o = o;
+    a.lse = lse;
+    a.N = N;
+    a.BH = BH;
+    a.d = d;
+    a.group = H / Hkv;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.status = ds->status;
+    cudaError_t e = launch_fwd_fp8(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
 extern "C" int fa_get_device_status(fa_stream_t stream) {
     DeviceState *ds = nullptr;
     int st = device_state(&ds);

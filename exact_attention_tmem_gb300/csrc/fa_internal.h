@@ -53,11 +53,30 @@ struct DecodeArgs {
     unsigned int *status;
 };
 
-// Kernel launchers (fa_fwd.cu, fa_bwd.cu, fa_decode.cu).  They return the launch's cudaError_t.
+// FP8 forward: Q and K codes [B*H|B*Hkv, N, d] e4m3, V codes transposed [B*Hkv, d, Npad],
+// per-head descale factors; O bf16, L fp32.
+struct Fp8FwdArgs {
+    CUtensorMap tm_q, tm_k, tm_vt;
+    const float *dsc_q, *dsc_k, *dsc_v;
+    void *o;
+    float *lse;
+    int N, BH, d, group;
+    float scale;
+    int causal;
+    unsigned int *status;
+};
+
+// Kernel launchers (fa_fwd.cu, fa_bwd.cu, fa_decode.cu, fa_fp8.cu).  They return the launch's cudaError_t.
 cudaError_t launch_fwd_bf16(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd_bf16(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const Fp8FwdArgs &a, cudaStream_t stream);
+// descale doubles as the per-head amax scratch while the kernels run
+cudaError_t launch_quantize_qk_fp8(const void *x, const float *signs, void *x8, float *descale, int BH, int N,
+                                   int d, cudaStream_t stream);
+cudaError_t launch_quantize_v_fp8(const void *v, void *vt8, float *descale, int BH, int N, int Npad, int d,
+                                  cudaStream_t stream);
 
 // Tile geometry shared by host and device code.
 constexpr int kTileRows = 128;     // rows of Q, K, V per tile

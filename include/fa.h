@@ -187,6 +187,57 @@ int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse,
               void *workspace, size_t workspace_bytes, int B, int H, int Hkv, int Nk,
               int d, float scale, int num_chunks, fa_stream_t stream);
 
+/*
+ * FP8 forward with incoherent processing.  The pages give only the idea ("FlashAttention"
+ * deep dive, section "How it works": fp8 with incoherent processing; "FlashAttention
+ * Explained", section "Later versions": an FP8 low-precision mode); the reading taken:
+ * e4m3 codes (round to nearest even, saturating at +-448) with one scale per
+ * (batch, head); Q and K rows rotated by the same orthogonal diag(s) H / sqrt(d) (H the
+ * Sylvester Hadamard matrix, s random signs drawn by the caller), which leaves Q K^T
+ * unchanged and spreads outlier coordinates before rounding.
+ */
+
+/* Bytes of the transposed V codes for [B,H,N,d]: B*H*d*Npad, Npad = N rounded up to 16. */
+size_t fa_fp8_v_bytes(int B, int H, int N, int d);
+
+/*
+ * Quantize Q or K for fa_fwd_fp8.
+ *   x        [B,H,N,d] bf16, read only
+ *   signs    d fp32 values of +-1 (device), or NULL for no rotation; use the same
+ *            signs for Q and K.  With signs each row becomes (x o signs) H / sqrt(d),
+ *            computed with the Walsh-Hadamard butterflies in fp32
+ *   x8       [B,H,N,d] e4m3 codes, written
+ *   descale  [B,H] fp32, written: amax / 448 of each (batch, head) slice (1/448 for an
+ *            all-zero slice); codes = e4m3(x * (448 / amax))
+ * d = 64 or 128.  Status codes as for fa_fwd.
+ */
+int fa_quantize_qk_fp8(const void *x, const float *signs, void *x8, float *descale, int B,
+                       int H, int N, int d, fa_stream_t stream);
+
+/*
+ * Quantize V for fa_fwd_fp8: e4m3 codes with one scale per (batch, head), transposed
+ *   v        [B,H,N,d] bf16, read only
+ *   vt8      [B,H,d,Npad] e4m3 codes (keys contiguous; keys N..Npad-1 are zero codes),
+ *            fa_fp8_v_bytes(B,H,N,d) bytes, written
+ *   descale  [B,H] fp32, written as for fa_quantize_qk_fp8
+ */
+int fa_quantize_v_fp8(const void *v, void *vt8, float *descale, int B, int H, int N, int d,
+                      fa_stream_t stream);
+
+/*
+ * FP8 forward: O = softmax(scale * (dq Q8)(dk K8)^T [causal]) (dv V8) with both products
+ * on the tensor cores in e4m3 (P rounded to e4m3 before the second product; the row
+ * sums stay in fp32).
+ *   q8            [B,H,N,d] e4m3 codes, k8 [B,Hkv,N,d], vt8 [B,Hkv,d,Npad] (as written by
+ *                 the quantize calls above; Q and K rotated alike or not at all)
+ *   descale_q     [B,H] fp32; descale_k, descale_v [B,Hkv] fp32
+ *   o             [B,H,N,d] bf16, written;  lse [B,H,N] fp32 natural log, written
+ * d = 128 only (FA_ERR_UNSUPPORTED otherwise); Hkv divides H.
+ */
+int fa_fwd_fp8(const void *q8, const void *k8, const void *vt8, const float *descale_q,
+               const float *descale_k, const float *descale_v, void *o, float *lse, int B,
+               int H, int Hkv, int N, int d, float scale, int causal, fa_stream_t stream);
+
 /* Size in bytes of the scratch array built into the library for fa_bwd_noalloc. */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 

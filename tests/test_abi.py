@@ -255,3 +255,29 @@ def test_decode_valid_call_without_gpu_reports_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert dec(lib) == _lib.FA_ERR_CUDA
+
+
+def test_fp8_host_checks(lib):
+    assert lib.fa_fp8_v_bytes(2, 3, 100, 128) == 2 * 3 * 128 * 112
+    assert lib.fa_fp8_v_bytes(1, 1, 16, 96) == 0
+    s = ctypes.c_float(0.1)
+    # null pointers
+    assert lib.fa_quantize_qk_fp8(None, None, A, A, 1, 1, 128, 128, None) == _lib.FA_ERR_INVALID_ARG
+    assert lib.fa_quantize_v_fp8(A, None, A, 1, 1, 128, 128, None) == _lib.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_fp8(A, A, A, A, A, None, A, A, 1, 1, 1, 128, 128, s, 1, None) == _lib.FA_ERR_INVALID_ARG
+    # shapes, head dims, alignment
+    assert lib.fa_quantize_qk_fp8(A, None, A, A, 1, 1, 128, 96, None) == _lib.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd_fp8(A, A, A, A, A, A, A, A, 1, 1, 1, 128, 64, s, 1, None) == _lib.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd_fp8(A, A, A, A, A, A, A, A, 1, 4, 3, 128, 128, s, 1, None) == _lib.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_fp8(A + 8, A, A, A, A, A, A, A, 1, 1, 1, 128, 128, s, 1, None) == _lib.FA_ERR_ALIGNMENT
+    assert lib.fa_quantize_qk_fp8(A, A + 2, A, A, 1, 1, 128, 128, None) == _lib.FA_ERR_ALIGNMENT
+    assert lib.fa_fwd_fp8(A, A, A, A, A, A, A, A, 1, 1, 1, 128, 128, ctypes.c_float(float("nan")), 1,
+                          None) == _lib.FA_ERR_INVALID_ARG
+
+
+def test_fp8_valid_calls_without_gpu_report_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.fa_quantize_qk_fp8(A, None, A, A, 1, 1, 128, 128, None) == _lib.FA_ERR_CUDA
+    assert lib.fa_fwd_fp8(A, A, A, A, A, A, A, A, 1, 1, 1, 128, 128, ctypes.c_float(0.1), 1, None) == _lib.FA_ERR_CUDA
