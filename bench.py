@@ -205,6 +205,105 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+FP8_METRIC = "attention TFLOPS (fwd), fp8 e4m3 with incoherent processing, N=8k d=128 causal (fa_fwd_fp8)"
+FP8_NOMINAL_RATIO = 2.0   # dense fp8 / dense bf16 tensor rate (4.5 / 2.25 PFLOP/s nominal)
+
+
+def run_fp8(args, world, rank, local):
+    """FP8 forward on workload 3's shape: Q and K rotated and quantized, V quantized and
+    transposed, outside the timed region (a model would keep them in fp8); the timed call
+    is fa_fwd_fp8.  The peak is the measured bf16 peak times the nominal fp8/bf16 ratio."""
+    import torch
+    import numpy as np
+    import exact_attention_tmem_gb300 as fa
+    from exact_attention_tmem_gb300 import inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.build()
+    w = inputs.WORKLOADS[WORKLOAD_ID]
+    B, H, N, d = args.shape if args.shape else (w.B, w.H, w.N, w.d)
+    if args.shape:
+        q_h, k_h, v_h = inputs.random_inputs(B, H, N, d, seed=WORKLOAD_ID)
+    else:
+        q_h, k_h, v_h = inputs.workload_inputs(WORKLOAD_ID)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    signs = torch.from_numpy(np.random.default_rng(41).choice([-1.0, 1.0], size=d).astype(np.float32)).to(dev)
+    q8, dq = fa.quantize_qk_fp8(q, signs)
+    k8, dk = fa.quantize_qk_fp8(k, signs)
+    vt8, dv = fa.quantize_v_fp8(v)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        fa.fwd_fp8(q8, k8, vt8, dq, dk, dv, causal=CAUSAL, out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        call()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    status = fa.device_status()
+    total_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in ev), dev)
+    flops = 4.0 * N * N * d * B * H / (2 if CAUSAL else 1)
+    value = job_tflops(world, args.steps, flops, total_ms)
+    e2e = None
+    if not args.no_e2e:
+        # the codes come from pinned host memory, O and L go back
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q8, k8, vt8))
+        ho = torch.empty(tuple(o.shape), dtype=torch.bfloat16).pin_memory()
+        hl = torch.empty(tuple(lse.shape), dtype=torch.float32).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            for dst, src in ((q8, hq), (k8, hk), (vt8, hv)):
+                dst.copy_(src, non_blocking=True)
+            call()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / args.steps
+        e2e = {"value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(t.numel() for t in (hq, hk, hv)),
+               "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4, "ms_per_step": ms}
+    if rank != 0:
+        return
+    peak_burst, _, _, peak_src = peaks()
+    peak8 = peak_burst * FP8_NOMINAL_RATIO
+    tf = value / world
+    line = {
+        "metric": FP8_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
+        "config": {"workload": f"fwd fp8 causal B={B} H={H} N={N} d={d}", "B": B, "H": H, "N": N, "d": d,
+                   "causal": CAUSAL, "scale": "1/sqrt(d)", "inputs": "workload 3's bf16 inputs, Q and K rotated by "
+                   "diag(s) H / sqrt(d) (signs seed 41), e4m3 codes with one scale per head",
+                   "l2": "inputs > L2; L2 flushed (256 MiB write) between timed calls",
+                   "parallelism": "one independent replica per GPU"},
+        "roofline": {"bound": "tensor", "kernel": "fwd_fp8_kernel (CUDA events around the C-ABI call)",
+                     "achieved": tf, "peak": peak8, "unit": "TFLOP/s", "frac": tf / peak8, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 burst x {FP8_NOMINAL_RATIO:g} (nominal fp8/bf16 ratio)"},
+        "e2e": e2e, "gpu_launches": args.steps, "device_status": status, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 DECODE_METRIC = "decode K/V read bandwidth, bf16, one query row per head (fa_decode)"
 DECODE_SHAPE = (8, 32, 32, 32768, 128)     # B, H, Hkv, Nk, d
 
@@ -471,6 +570,8 @@ def main():
                     help="skip timing the fp64 oracle on the host")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the FP8 forward (fa_fwd_fp8) on the same shape instead of the bf16 step")
     ap.add_argument("--decode", action="store_true",
                     help="time the decoding kernel (one query row per head) instead of the fwd+bwd step")
     ap.add_argument("--decode-shape", type=lambda x: tuple(int(v) for v in x.split(",")), default=None,
@@ -491,6 +592,8 @@ def main():
         world, rank, local = dist_setup("nccl")
         if args.decode:
             run_decode(args, world, rank, local)
+        elif args.fp8:
+            run_fp8(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     if world > 1:
