@@ -25,6 +25,9 @@ enum : unsigned int { kStatusTimeout = 1u };
 // Upper bound for any single wait inside a kernel.  Legitimate waits last
 // microseconds; one second means the pipeline is broken.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+// Longest sleep of one polling step inside a wait (the thread wakes when the phase
+// completes); well below the limit so that the abort flag and clock are rechecked.
+constexpr uint32_t kWaitSleepNs = 20000;
 
 // Per-CTA context of the bounded waits: the shared abort flag that makes every role
 // wind down once one wait has given up, and the device status word.
@@ -76,6 +79,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in the barrier unit (issuing
+// nothing) until the phase completes or about `ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Slow path of mbar_wait: keeps polling until the phase completes, the CTA's abort
 // flag is raised by another thread, or the time limit passes (then raises the flag
 // and records `site` in the device status word).
@@ -85,7 +102,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
                                             bool honour_abort) {
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
         if ((it & 31u) == 0) {
             if (honour_abort && *ctx.abort_flag) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
