@@ -284,23 +284,47 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 return s;
             };
             auto issue_qk = [&](int t, int s) {
+                if constexpr (!C::kTF32 && (C::kQKSteps == 4 || C::kQKSteps == 8)) {
+                    // bf16: the whole product from one asm block
+                    const uint64_t a0 = sdesc_sw128(sQ + t * C::kTileBytes, 16, 1024);
+                    const uint64_t b0 = sdesc_sw128(sKV + s * C::kTileBytes, 16, 1024);
+                    uint64_t a[C::kQKSteps], b[C::kQKSteps];
 #pragma unroll
-                for (int kk = 0; kk < C::kQKSteps; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32;
-                    const uint64_t a = sdesc_sw128(sQ + t * C::kTileBytes + off, 16, 1024);
-                    const uint64_t b = sdesc_sw128(sKV + s * C::kTileBytes + off, 16, 1024);
-                    umma_ss<C::kTF32>(tS[t], a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < C::kQKSteps; ++kk) {
+                        const uint32_t off = (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32;
+                        a[kk] = sdesc_step(a0, off);
+                        b[kk] = sdesc_step(b0, off);
+                    }
+                    if constexpr (C::kQKSteps == 8) umma_f16_ss_x8(tS[t], a, b, C::kIdescQK, 0u);
+                    else umma_f16_ss_x4(tS[t], a, b, C::kIdescQK, 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < C::kQKSteps; ++kk) {
+                        const uint32_t off = (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32;
+                        const uint64_t a = sdesc_sw128(sQ + t * C::kTileBytes + off, 16, 1024);
+                        const uint64_t b = sdesc_sw128(sKV + s * C::kTileBytes + off, 16, 1024);
+                        umma_ss<C::kTF32>(tS[t], a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    }
                 }
             };
             auto issue_pv = [&](int t, int s, bool acc) {
+                if constexpr (!C::kTF32 && C::kPVSteps == 8) {
+                    // bf16: V as an MN-major B operand, 16 key rows (2 KB) per step
+                    const uint64_t b0 = sdesc_sw128(sKV + s * C::kTileBytes, C::kBoxTileBytes, 1024);
+                    uint64_t b[8];
 #pragma unroll
-                for (int kk = 0; kk < C::kPVSteps; ++kk) {
-                    // bf16: V as an MN-major B operand; TF32: V^T as a K-major B operand
-                    const uint64_t b =
-                        C::kTF32 ? sdesc_sw128(base + C::kVtOff + (kk >> 2) * C::kVtBoxBytes + (kk & 3) * 32, 16, 1024)
-                                 : sdesc_sw128(sKV + s * C::kTileBytes + kk * C::kKStep * kBoxBytes,
-                                               C::kBoxTileBytes, 1024);
-                    umma_ts<C::kTF32>(tO[t], tS[t] + kk * 8u, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 8; ++kk) b[kk] = sdesc_step(b0, kk * C::kKStep * kBoxBytes);
+                    umma_f16_ts_x8(tO[t], tS[t], b, C::kIdescPV, acc ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < C::kPVSteps; ++kk) {
+                        // TF32: V^T as a K-major B operand
+                        const uint64_t b =
+                            C::kTF32 ? sdesc_sw128(base + C::kVtOff + (kk >> 2) * C::kVtBoxBytes + (kk & 3) * 32, 16, 1024)
+                                     : sdesc_sw128(sKV + s * C::kTileBytes + kk * C::kKStep * kBoxBytes,
+                                                   C::kBoxTileBytes, 1024);
+                        umma_ts<C::kTF32>(tO[t], tS[t] + kk * 8u, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                    }
                 }
             };
             bool ok = mbar_wait_w(bar(B::kQ), 0, kSiteMmaQ);

@@ -339,6 +339,66 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
             : "memory");
     }
 }
+// Whole bf16 products issued from one asm block (warp-collective, lane 0 issues): the
+// K steps' descriptors come in as arrays (see sdesc_step), the first step accumulates
+// only if `accumulate` is non-zero, the rest always do.  TS forms step the A operand by
+// 8 tensor-memory columns (16 bf16 K elements) per step.  Fewer instructions per
+// product than one call per step, which matters because the MMA warp shares its
+// sub-partition with softmax warps.
+__device__ __forceinline__ void umma_f16_ss_x4(uint32_t d_tmem, const uint64_t (&a)[4], const uint64_t (&b)[4],
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t, e;\n\t.reg .b32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "setp.ne.b32 p, %2, 0;\n\tsetp.eq.u32 t, l, l;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %1, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %10, %1, t;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(idesc), "r"(accumulate), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
+        : "memory");
+}
+__device__ __forceinline__ void umma_f16_ss_x8(uint32_t d_tmem, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t, e;\n\t.reg .b32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "setp.ne.b32 p, %2, 0;\n\tsetp.eq.u32 t, l, l;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %1, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %17, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %10, %18, %1, t;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(idesc), "r"(accumulate), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
+        : "memory");
+}
+__device__ __forceinline__ void umma_f16_ts_x8(uint32_t d_tmem, uint32_t a_tmem, const uint64_t (&b)[8],
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t, e;\n\t.reg .b32 l, ta;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "setp.ne.b32 p, %3, 0;\n\tsetp.eq.u32 t, l, l;\n\t"
+        "add.u32 ta, %1, 0;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %4, %2, p;\n\t"
+        "add.u32 ta, %1, 8;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %5, %2, t;\n\t"
+        "add.u32 ta, %1, 16;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %6, %2, t;\n\t"
+        "add.u32 ta, %1, 24;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %7, %2, t;\n\t"
+        "add.u32 ta, %1, 32;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %8, %2, t;\n\t"
+        "add.u32 ta, %1, 40;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %9, %2, t;\n\t"
+        "add.u32 ta, %1, 48;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %10, %2, t;\n\t"
+        "add.u32 ta, %1, 56;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %11, %2, t;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(idesc), "r"(accumulate), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
+        : "memory");
+}
+
+// Descriptor `desc` with its start-address field (16-byte units, low 14 bits) advanced
+// by `bytes`; shared addresses stay below 256 KB, so no carry leaves the field.
+__device__ __forceinline__ uint64_t sdesc_step(uint64_t desc, uint32_t bytes) {
+    return (desc & 0xFFFFFFFF00000000ull) | static_cast<uint32_t>(static_cast<uint32_t>(desc) + (bytes >> 4));
+}
+
 // kind::f8f6f4 (8-bit A and B, fp32 accumulator), warp-collective like umma_ss/umma_ts.
 __device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                            uint32_t accumulate) {
