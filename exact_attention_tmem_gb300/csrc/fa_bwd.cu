@@ -354,22 +354,27 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tc_fence_after();
                 return s;
             };
-            // K-major x K-major product over the head dim: D[128 x 128] = A B^T
+            // K-major x K-major product over the head dim: D[128 x 128] = A B^T (each
+            // product goes out from one asm block; see umma_f16_ss_x8)
             auto mma_kk = [&](uint32_t d_tmem, uint32_t a_s, uint32_t b_s) {
+                const uint64_t a0 = sdesc_sw128(a_s, 16, 1024), b0 = sdesc_sw128(b_s, 16, 1024);
+                uint64_t a[C::kKSteps], b[C::kKSteps];
 #pragma unroll
                 for (int kk = 0; kk < C::kKSteps; ++kk) {
                     const uint32_t off = (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32;
-                    umma_ss(d_tmem, sdesc_sw128(a_s + off, 16, 1024), sdesc_sw128(b_s + off, 16, 1024),
-                                  C::kIdescSS, kk > 0 ? 1u : 0u);
+                    a[kk] = sdesc_step(a0, off);
+                    b[kk] = sdesc_step(b0, off);
                 }
+                if constexpr (C::kKSteps == 8) umma_f16_ss_x8(d_tmem, a, b, C::kIdescSS, 0u);
+                else umma_f16_ss_x4(d_tmem, a, b, C::kIdescSS, 0u);
             };
-            // A from TMEM (128 x 128, bf16 packed), B MN-major [128 rows x D]
+            // A from TMEM (128 x 128, bf16 packed), B MN-major [128 rows x D], 16 rows per step
             auto mma_tn = [&](uint32_t d_tmem, uint32_t a_tmem, uint32_t b_s, bool acc) {
+                const uint64_t b0 = sdesc_sw128(b_s, C::kBoxTileBytes, 1024);
+                uint64_t b[C::kRowSteps];
 #pragma unroll
-                for (int kk = 0; kk < C::kRowSteps; ++kk)
-                    umma_ts(d_tmem, a_tmem + kk * 8u,
-                                  sdesc_sw128(b_s + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024), C::kIdescTS,
-                                  (acc || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < C::kRowSteps; ++kk) b[kk] = sdesc_step(b0, kk * 16 * kBoxBytes);
+                umma_f16_ts_x8(d_tmem, a_tmem, b, C::kIdescTS, acc ? 1u : 0u);
             };
             bool ok = mbar_wait_w(bar(B::kKV), 0, kSiteBMmaKV);
             tc_fence_after();
@@ -417,11 +422,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tc_fence_after();
                     mma_tn(tDK, tDP, sQ + qs_it * C::kTileBytes, it > 0);
                     umma_commit(bar(B::kQEmpty + qs_it));
+                    {
+                        const uint64_t a0 = sdesc_sw128(sDS, C::kBoxTileBytes, 1024);
+                        const uint64_t b0 = sdesc_sw128(sK, C::kBoxTileBytes, 1024);
+                        uint64_t a[C::kRowSteps], b[C::kRowSteps];
 #pragma unroll
-                    for (int kk = 0; kk < C::kRowSteps; ++kk)
-                        umma_ss(tDP, sdesc_sw128(sDS + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024),
-                                      sdesc_sw128(sK + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024), C::kIdescDQ,
-                                      kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < C::kRowSteps; ++kk) {
+                            a[kk] = sdesc_step(a0, kk * 16 * kBoxBytes);
+                            b[kk] = sdesc_step(b0, kk * 16 * kBoxBytes);
+                        }
+                        umma_f16_ss_x8(tDP, a, b, C::kIdescDQ, 0u);
+                    }
                     umma_commit(bar(B::kDQFull));
                     if (it + 1 < n_it) {
                         // dV += P^T dO_{i+1} (P^T from the S^T columns)
@@ -863,12 +874,16 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             auto active = [&](int t, int j) { return j < ntile[t]; };
             // S_t = A_t B^T over the head dim; A_t = Q_t or dO_t, B = K_j or V_j (both K-major)
             auto mma_rows = [&](uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile) {
+                const uint64_t a0 = sdesc_sw128(a_tile, 16, 1024), b0 = sdesc_sw128(b_tile, 16, 1024);
+                uint64_t a[C::kKSteps], b[C::kKSteps];
 #pragma unroll
                 for (int kk = 0; kk < C::kKSteps; ++kk) {
                     const uint32_t off = (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32;
-                    umma_ss(d_tmem, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(b_tile + off, 16, 1024),
-                                  C::kIdescS, kk > 0 ? 1u : 0u);
+                    a[kk] = sdesc_step(a0, off);
+                    b[kk] = sdesc_step(b0, off);
                 }
+                if constexpr (C::kKSteps == 8) umma_f16_ss_x8(d_tmem, a, b, C::kIdescS, 0u);
+                else umma_f16_ss_x4(d_tmem, a, b, C::kIdescS, 0u);
             };
             auto wait_k = [&](int j) -> int {
                 const int s = j % C::kKStages;
@@ -918,11 +933,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     // dQ_t += dS_t K_j, then S_t for the next key block into the same columns
                     if (!mbar_wait_w(bar(B::kDSFull + t), j & 1, kSiteQMmaDS)) { ok = false; break; }
                     tc_fence_after();
+                    {
+                        const uint64_t b0 = sdesc_sw128(sK + ks * C::kTileBytes, C::kBoxTileBytes, 1024);
+                        uint64_t b[C::kRowSteps];
 #pragma unroll
-                    for (int kk = 0; kk < C::kRowSteps; ++kk)
-                        umma_ts(tDQ[t], tSD[t] + kk * 8u,
-                                      sdesc_sw128(sK + ks * C::kTileBytes + kk * 16 * kBoxBytes, C::kBoxTileBytes, 1024),
-                                      C::kIdescDQ, (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < C::kRowSteps; ++kk) b[kk] = sdesc_step(b0, kk * 16 * kBoxBytes);
+                        umma_f16_ts_x8(tDQ[t], tSD[t], b, C::kIdescDQ, j > 0 ? 1u : 0u);
+                    }
                     if (active(t, j + 1)) {
                         if (ks_next < 0) ks_next = wait_k(j + 1);
                         if (ks_next < 0) { ok = false; break; }

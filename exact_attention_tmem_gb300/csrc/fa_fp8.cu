@@ -332,17 +332,24 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tc_fence_after();
                 return s;
             };
+            static_assert(C::kKSteps == 4 && C::kPVSteps == 4, "4-step products");
             auto issue_qk = [&](int t, int s) {
+                const uint64_t a0 = sdesc_sw128(sQ + t * C::kTileBytes, 16, 1024);
+                const uint64_t b0 = sdesc_sw128(sKV + s * C::kTileBytes, 16, 1024);
+                uint64_t a[4], b[4];
 #pragma unroll
-                for (int kk = 0; kk < C::kKSteps; ++kk)
-                    umma_ss_f8(tS[t], sdesc_sw128(sQ + t * C::kTileBytes + kk * 32, 16, 1024),
-                               sdesc_sw128(sKV + s * C::kTileBytes + kk * 32, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk) {
+                    a[kk] = sdesc_step(a0, kk * 32);
+                    b[kk] = sdesc_step(b0, kk * 32);
+                }
+                umma_f8_ss_x4(tS[t], a, b, C::kIdescQK, 0u);
             };
             auto issue_pv = [&](int t, int s, bool acc) {
+                const uint64_t b0 = sdesc_sw128(sKV + s * C::kTileBytes, 16, 1024);
+                uint64_t b[4];
 #pragma unroll
-                for (int kk = 0; kk < C::kPVSteps; ++kk)
-                    umma_ts_f8(tO[t], tS[t] + kk * 8u, sdesc_sw128(sKV + s * C::kTileBytes + kk * 32, 16, 1024),
-                               C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk) b[kk] = sdesc_step(b0, kk * 32);
+                umma_f8_ts_x4(tO[t], tS[t], b, C::kIdescPV, acc ? 1u : 0u);
             };
             bool ok = mbar_wait_w(bar(B::kQ), 0, kSite8MmaQ);
             if (ok) {

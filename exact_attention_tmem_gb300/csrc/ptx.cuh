@@ -393,6 +393,46 @@ __device__ __forceinline__ void umma_f16_ts_x8(uint32_t d_tmem, uint32_t a_tmem,
         : "memory");
 }
 
+__device__ __forceinline__ void umma_f16_ts_x4(uint32_t d_tmem, uint32_t a_tmem, const uint64_t (&b)[4],
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t, e;\n\t.reg .b32 l, ta;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "setp.ne.b32 p, %3, 0;\n\tsetp.eq.u32 t, l, l;\n\t"
+        "add.u32 ta, %1, 0;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %4, %2, p;\n\t"
+        "add.u32 ta, %1, 8;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %5, %2, t;\n\t"
+        "add.u32 ta, %1, 16;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %6, %2, t;\n\t"
+        "add.u32 ta, %1, 24;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %7, %2, t;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(idesc), "r"(accumulate), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
+        : "memory");
+}
+__device__ __forceinline__ void umma_f8_ss_x4(uint32_t d_tmem, const uint64_t (&a)[4], const uint64_t (&b)[4],
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t, e;\n\t.reg .b32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "setp.ne.b32 p, %2, 0;\n\tsetp.eq.u32 t, l, l;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %7, %1, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %8, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %5, %9, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %6, %10, %1, t;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(idesc), "r"(accumulate), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
+        : "memory");
+}
+__device__ __forceinline__ void umma_f8_ts_x4(uint32_t d_tmem, uint32_t a_tmem, const uint64_t (&b)[4],
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t, e;\n\t.reg .b32 l, ta;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+        "setp.ne.b32 p, %3, 0;\n\tsetp.eq.u32 t, l, l;\n\t"
+        "add.u32 ta, %1, 0;\n\t@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], %4, %2, p;\n\t"
+        "add.u32 ta, %1, 8;\n\t@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], %5, %2, t;\n\t"
+        "add.u32 ta, %1, 16;\n\t@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], %6, %2, t;\n\t"
+        "add.u32 ta, %1, 24;\n\t@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], %7, %2, t;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(idesc), "r"(accumulate), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
+        : "memory");
+}
+
 // Descriptor `desc` with its start-address field (16-byte units, low 14 bits) advanced
 // by `bytes`; shared addresses stay below 256 KB, so no carry leaves the field.
 __device__ __forceinline__ uint64_t sdesc_step(uint64_t desc, uint32_t bytes) {
