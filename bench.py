@@ -80,8 +80,70 @@ def peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+class NvmlPoller:
+    """SM clock and clock-event reasons read through NVML (read-only queries) every
+    few milliseconds from a host thread, so that even a timed region of a few
+    milliseconds holds several samples.  The device is matched by UUID."""
+    SM = 1                           # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid, index, period_s=0.002):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        rc = 1
+        if uuid:
+            rc = self.lib.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(self.h))
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError("no NVML handle for the device")
+        self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(
+            self.h, self.SM, ctypes.byref(mx)) == 0 else None
+        self.period = period_s
+        self.samples, self.reasons = [], set()
+        self.stop_ev = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        ct = self.ct
+        mhz, bits = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop_ev.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, ct.byref(mhz)) == 0:
+                self.samples.append(float(mhz.value))
+            if self.reason_fn(self.h, ct.byref(bits)) == 0:
+                for bit, name in self.REASONS.items():
+                    if bits.value & bit:
+                        self.reasons.add(name)
+            self.stop_ev.wait(self.period)
+
+    def start(self):
+        self.thread.start()
+
+    def stop(self):
+        self.stop_ev.set()
+        self.thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+
+    def summary(self):
+        if not self.samples:
+            return None
+        return {"sm_mhz": statistics.median(self.samples),
+                "sm_max_mhz": self.max_mhz if self.max_mhz else max(self.samples),
+                "samples": len(self.samples), "source": "nvml", "reasons": sorted(self.reasons)}
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+    """Clocks and throttle reasons of the bench's GPU during the timed region: NVML
+    polled from a host thread, else nvidia-smi sampled every 200 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -90,13 +152,29 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = None
+        self.nvml = None
+
+    def _uuid(self):
+        try:
+            import torch
+            return str(torch.cuda.get_device_properties(self.index).uuid)
+        except Exception:
+            return None
 
     def __enter__(self):
         try:
+            self.nvml = NvmlPoller(self._uuid(), self.index)
+            self.nvml.start()
+            return self
+        except (OSError, AttributeError):
+            self.nvml = None
+        try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
+            dev_id = self._uuid()
+            dev_id = ("GPU-" + dev_id) if dev_id else str(self.index)
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", f"--id={dev_id}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
                 stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except OSError:
@@ -104,6 +182,8 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
+        if self.nvml is not None:
+            self.nvml.stop()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -112,6 +192,8 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        if self.nvml is not None:
+            return self.nvml.summary()
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return None
         rows = list(csv.reader(io.StringIO(open(self.path).read())))
@@ -132,7 +214,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "source": "nvidia-smi", "reasons": sorted(reasons)}
 
 
 def dist_setup(backend):
