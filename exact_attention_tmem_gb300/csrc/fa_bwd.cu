@@ -231,8 +231,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / nkv;         // key/value head
-    const int j = blockIdx.x % nkv;          // key block; j = 0 (the longest walk) first
+    int bh, j;                               // key/value head, key block
+    heavy_first_order(blockIdx.x, nkv, bh, j);   // j = 0 (the longest causal walk) first
     const int nq = Npad / kTileRows;
     const int i0 = causal ? j : 0;
     const int n_q = nq - i0;                 // query blocks per query head (>= 1)
@@ -773,9 +773,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / num_pairs;            // query head
+    int bh, rank;                                     // query head, pair rank
+    heavy_first_order(blockIdx.x, num_pairs, bh, rank);
     const int bh_kv = bh / group;                     // its key/value head
-    const int rank = blockIdx.x % num_pairs;
     const int pair = causal ? (num_pairs - 1 - rank) : rank;   // longest walks first
     const int nkv = (N + kTileRows - 1) / kTileRows;
     int ntile[2];                                     // key blocks each query tile visits

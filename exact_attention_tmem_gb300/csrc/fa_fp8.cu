@@ -253,9 +253,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / num_pairs;
+    int bh, rank;
+    heavy_first_order(blockIdx.x, num_pairs, bh, rank);
     const int bh_kv = bh / group;
-    const int rank = blockIdx.x % num_pairs;
     const int pair = causal ? (num_pairs - 1 - rank) : rank;
     const int nkv = (N + kTileRows - 1) / kTileRows;
     int ntile[2];

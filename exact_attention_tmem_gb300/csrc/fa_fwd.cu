@@ -131,11 +131,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / num_pairs;
+    int bh, rank;
+    heavy_first_order(blockIdx.x, num_pairs, bh, rank);
     // grouped-query attention: `group` query heads share one key/value head
     const int bh_kv = bh / group;
-    const int rank = blockIdx.x % num_pairs;
-    // heaviest group of query tiles first within a head when causal
+    // rank 0 is the heaviest group of query tiles of a head when causal
     const int pair = causal ? (num_pairs - 1 - rank) : rank;
     const int nkv = (N + kTileRows - 1) / kTileRows;
     int ntile[2];

@@ -47,6 +47,25 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 
 // ---------------------------------------------------------------------------------
+// launch order of attention work items
+// ---------------------------------------------------------------------------------
+// A grid of num_heads x per_head CTAs, where rank 0 of a head is its longest walk
+// (causal work) is taken in groups of kHeadGroup heads, rank-major inside a group:
+// rank 0 of every head of the group, then rank 1, ...  The longest walks of a group
+// start first, so the last CTAs of the grid are short ones (no long tail on a few
+// SMs), while the group's heads alone are in flight and their tiles stay in L2.
+constexpr int kHeadGroup = 8;
+__device__ __forceinline__ void heavy_first_order(int idx, int per_head, int &head, int &rank) {
+    const int num_heads = static_cast<int>(gridDim.x) / per_head;
+    const int per_group = kHeadGroup * per_head;
+    const int g = idx / per_group;
+    const int r = idx - g * per_group;
+    const int heads_here = min(kHeadGroup, num_heads - g * kHeadGroup);
+    rank = r / heads_here;
+    head = g * kHeadGroup + r % heads_here;
+}
+
+// ---------------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
