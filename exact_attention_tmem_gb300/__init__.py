@@ -16,7 +16,7 @@ import torch
 from . import _lib
 from ._lib import FaError  # noqa: F401
 
-__all__ = ["fwd", "bwd", "decode", "quantize_qk_fp8", "quantize_v_fp8", "fwd_fp8", "bwd_workspace_size",
+__all__ = ["fwd", "bwd", "fwd_bwd_host", "fwd_bwd_host_buffer_size", "decode", "quantize_qk_fp8", "quantize_v_fp8", "fwd_fp8", "bwd_workspace_size",
            "bwd_deterministic_workspace_size", "decode_workspace_size", "device_status", "build", "FaError"]
 
 
@@ -138,6 +138,57 @@ def bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
         st, name = lib.fa_bwd_gqa(*args, B, H, Hkv, N, d, scale, int(bool(causal)), stream), "fa_bwd_gqa"
     _lib.check(st, name)
     return dq, dk, dv
+
+
+def fwd_bwd_host_buffer_size(B: int, H: int, N: int, d: int, chunk_heads: int = 0) -> int:
+    return int(_lib.load().fa_fwd_bwd_host_buffer_size(B, H, N, d, chunk_heads))
+
+
+def fwd_bwd_host(q, k, v, do, causal: bool = False, scale: float | None = None, o=None, lse=None,
+                 dq=None, dk=None, dv=None, buffer=None, chunk_heads: int = 0, device=None):
+    """Forward then backward on tensors in host memory (fa_fwd_bwd_host): the library
+    copies chunks of heads in, runs fa_fwd and fa_bwd on them and copies the results
+    out, overlapping the copies with the kernels.
+
+    q, k, v, do: [B, H, N, d] bf16 CPU tensors (page-locked for overlap).  Returns
+    (o, lse, dq, dk, dv) as CPU tensors; they are complete once the current stream of
+    ``device`` has been synchronised.  ``buffer`` is the device scratch of
+    fwd_bwd_host_buffer_size(B, H, N, d, chunk_heads) bytes (allocated if None).
+    """
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    B, H, N, d = q.shape
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+
+    def host(t, dtype, shape, name):
+        if t.is_cuda or t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dtype} CPU tensor of shape {tuple(shape)}")
+        return t
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("do", do)):
+        host(t, torch.bfloat16, q.shape, name)
+    pin = q.is_pinned()
+    o = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin) if lse is None else lse
+    dq = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin) if dq is None else dq
+    dk = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin) if dk is None else dk
+    dv = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin) if dv is None else dv
+    for name, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        host(t, torch.bfloat16, q.shape, name)
+    host(lse, torch.float32, (B, H, N), "lse")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    need = fwd_bwd_host_buffer_size(B, H, N, d, chunk_heads)
+    if buffer is None:
+        buffer = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    if not buffer.is_cuda:
+        raise ValueError("buffer must be a CUDA tensor")
+    lib = _lib.load()
+    st = lib.fa_fwd_bwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), buffer.data_ptr(),
+                             buffer.numel() * buffer.element_size(), B, H, N, d, scale, int(bool(causal)),
+                             int(chunk_heads), _stream_ptr(buffer.device))
+    _lib.check(st, "fa_fwd_bwd_host")
+    return o, lse, dq, dk, dv
 
 
 def decode_workspace_size(B: int, H: int, Hkv: int, Nk: int, d: int) -> int:

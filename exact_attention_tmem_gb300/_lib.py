@@ -24,6 +24,7 @@ FA_ERR_DEVICE_TIMEOUT = 6
 
 EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_gqa",
             "fa_bwd_deterministic_workspace_size", "fa_bwd_deterministic", "fa_bwd_noalloc",
+            "fa_fwd_bwd_host_buffer_size", "fa_fwd_bwd_host",
             "fa_decode_workspace_size", "fa_decode",
             "fa_fp8_v_bytes", "fa_quantize_qk_fp8", "fa_quantize_v_fp8", "fa_fwd_fp8",
             "fa_get_device_status", "fa_selftest_wait_timeout", "fa_status_string",
@@ -82,6 +83,10 @@ def load() -> ctypes.CDLL:
         lib.fa_fwd_fp8.restype = I
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, vp]
         lib.fa_bwd_noalloc.restype = I
+        lib.fa_fwd_bwd_host_buffer_size.argtypes = [I, I, I, I, I]
+        lib.fa_fwd_bwd_host_buffer_size.restype = Z
+        lib.fa_fwd_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, Z, I, I, I, I, F, I, I, vp]
+        lib.fa_fwd_bwd_host.restype = I
         lib.fa_get_device_status.argtypes = [vp]
         lib.fa_get_device_status.restype = I
         lib.fa_selftest_wait_timeout.argtypes = [vp]

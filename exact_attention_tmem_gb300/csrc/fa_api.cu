@@ -178,6 +178,10 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
 
 using namespace fa;
 
+namespace fa {
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+}  // namespace fa
+
 extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
                       int d, float scale, int causal, fa_stream_t stream) {
     return fwd_common(q, k, v, o, lse, B, H, H, N, d, scale, causal, reinterpret_cast<cudaStream_t>(stream),

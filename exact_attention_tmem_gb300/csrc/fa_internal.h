@@ -78,6 +78,10 @@ cudaError_t launch_quantize_qk_fp8(const void *x, const float *signs, void *x8, 
 cudaError_t launch_quantize_v_fp8(const void *v, void *vt8, float *descale, int BH, int N, int Npad, int d,
                                   cudaStream_t stream);
 
+// Records a failed CUDA call for fa_last_cuda_error() (this thread) and returns FA_ERR_CUDA
+// (fa_api.cu).
+int record_cuda_error(cudaError_t e);
+
 // Tile geometry shared by host and device code.
 constexpr int kTileRows = 128;     // rows of Q, K, V per tile
 constexpr int kBoxBytes = 128;     // inner extent of one TMA box (the 128-byte swizzle span)

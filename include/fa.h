@@ -265,6 +265,47 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
                    float scale, int causal, fa_stream_t stream);
 
 /*
+ * Bytes of device buffer fa_fwd_bwd_host needs: three slots, each holding one chunk
+ * of chunk_heads heads (q, k, v, dout, o, dq, dk, dv in bf16, lse in fp32, and the
+ * chunk's fa_bwd workspace), each part 256-byte aligned.  chunk_heads <= 0 picks
+ * ceil(B*H / 8); a value above B*H is clamped to B*H.  Returns 0 if the arguments
+ * are invalid.
+ */
+size_t fa_fwd_bwd_host_buffer_size(int B, int H, int N, int d, int chunk_heads);
+
+/*
+ * One training step of attention, forward then backward, on tensors in HOST memory:
+ * the same results as fa_fwd followed by fa_bwd on device copies of the inputs, with
+ * the host<->device copies overlapped with the kernels.  Every (batch, head) pair is
+ * an independent problem ("FlashAttention" deep dive, section "How it works": the
+ * inputs and outputs of one head, no state between calls), so the B*H heads are cut
+ * into chunks of chunk_heads consecutive heads; chunk c is copied in on an internal
+ * stream, computed on `stream` (even chunks) or an internal compute stream (odd
+ * chunks), and copied out on another internal stream, while chunks c - 1 and c + 1
+ * are being copied.
+ *   q, k, v, dout   [B,H,N,d] bf16, HOST memory, read only
+ *   o, dq, dk, dv   [B,H,N,d] bf16, HOST memory, written
+ *   lse             [B,H,N]   fp32, HOST memory, written
+ *   dev_buf         device buffer of at least fa_fwd_bwd_host_buffer_size(B, H, N, d,
+ *                   chunk_heads) bytes, 256-byte aligned, owned by the caller; scratch
+ * Host buffers should be page-locked (cudaHostAlloc or cudaHostRegister): copies from
+ * pageable memory are correct but do not overlap.  The call enqueues the work and
+ * returns; the results are in host memory once `stream` reaches the point of the
+ * call (synchronise `stream`).  Work enqueued earlier on `stream` happens before the
+ * first copy.  The library creates three streams and a few events per device on
+ * first use and reuses them; concurrent calls on one device are serialised while
+ * they enqueue, and must use distinct buffers.
+ * Returns the statuses of fa_fwd and fa_bwd (argument errors before anything is
+ * enqueued; FA_ERR_WORKSPACE if dev_buf is NULL or too small, FA_ERR_ALIGNMENT if it
+ * is not 256-byte aligned).  After a CUDA error part of the step may have been
+ * enqueued and the outputs are undefined.
+ */
+int fa_fwd_bwd_host(const void *q, const void *k, const void *v, const void *dout, void *o,
+                    float *lse, void *dq, void *dk, void *dv, void *dev_buf, size_t dev_buf_bytes,
+                    int B, int H, int N, int d, float scale, int causal, int chunk_heads,
+                    fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT if a kernel gave up
  * waiting since the last call (its outputs are then undefined).  Returns

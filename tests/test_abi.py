@@ -281,3 +281,53 @@ def test_fp8_valid_calls_without_gpu_report_cuda_error(lib):
         pytest.skip("a GPU is present")
     assert lib.fa_quantize_qk_fp8(A, None, A, A, 1, 1, 128, 128, None) == _lib.FA_ERR_CUDA
     assert lib.fa_fwd_fp8(A, A, A, A, A, A, A, A, 1, 1, 1, 128, 128, ctypes.c_float(0.1), 1, None) == _lib.FA_ERR_CUDA
+
+
+def host_step(lib, ptrs=None, buf=W, buf_bytes=None, B=1, H=2, N=128, d=128, scale=0.1, chunk=1):
+    ptrs = [A] * 9 if ptrs is None else ptrs
+    if buf_bytes is None:
+        buf_bytes = lib.fa_fwd_bwd_host_buffer_size(B, H, N, d, chunk)
+    return lib.fa_fwd_bwd_host(*ptrs, buf, buf_bytes, B, H, N, d, ctypes.c_float(scale), 1, chunk, None)
+
+
+def test_fwd_bwd_host_buffer_size(lib):
+    B, H, N, d = 2, 3, 300, 64
+    tensor = -(-(2 * N * d * 2) // 256) * 256           # a chunk of two heads, bf16
+    lse = -(-(2 * N * 4) // 256) * 256
+    ws = -(-lib.fa_bwd_workspace_size(1, 2, N, d) // 256) * 256
+    assert lib.fa_fwd_bwd_host_buffer_size(B, H, N, d, 2) == 3 * (8 * tensor + lse + ws)
+    # chunk_heads <= 0 takes ceil(B*H / 8) = 1 head; above B*H it is clamped
+    assert lib.fa_fwd_bwd_host_buffer_size(B, H, N, d, 0) == lib.fa_fwd_bwd_host_buffer_size(B, H, N, d, 1)
+    assert lib.fa_fwd_bwd_host_buffer_size(B, H, N, d, 99) == lib.fa_fwd_bwd_host_buffer_size(B, H, N, d, 6)
+    assert lib.fa_fwd_bwd_host_buffer_size(0, 1, 8, 64, 1) == 0
+    assert lib.fa_fwd_bwd_host_buffer_size(1, 1, 8, 96, 1) == 0
+
+
+@pytest.mark.parametrize("which", range(9))
+def test_fwd_bwd_host_null_pointer(lib, which):
+    ptrs = [A] * 9
+    ptrs[which] = None
+    assert host_step(lib, ptrs) == _lib.FA_ERR_INVALID_ARG
+
+
+def test_fwd_bwd_host_checks(lib):
+    assert host_step(lib, B=0, buf_bytes=1 << 30) == _lib.FA_ERR_INVALID_ARG
+    assert host_step(lib, d=96, buf_bytes=1 << 30) == _lib.FA_ERR_UNSUPPORTED
+    assert host_step(lib, scale=float("inf")) == _lib.FA_ERR_INVALID_ARG
+    assert host_step(lib, buf=None) == _lib.FA_ERR_WORKSPACE
+    need = lib.fa_fwd_bwd_host_buffer_size(1, 2, 128, 128, 1)
+    assert host_step(lib, buf_bytes=need - 1) == _lib.FA_ERR_WORKSPACE
+    assert host_step(lib, buf=W + 16) == _lib.FA_ERR_ALIGNMENT
+    # host pointers need no particular alignment
+    ptrs = [A + 1] * 9
+    import torch
+    if not torch.cuda.is_available():
+        assert host_step(lib, ptrs) == _lib.FA_ERR_CUDA
+
+
+def test_fwd_bwd_host_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert host_step(lib) == _lib.FA_ERR_CUDA
+    assert _lib.last_cuda_error() != 0
