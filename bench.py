@@ -43,10 +43,10 @@ REF_STEP_ROWS = 32      # query rows per head per step of the reference arm
 # they had when the counters were taken; after any change it reads as null until the
 # capture is repeated.
 TRAFFIC = {
-    "bwd": (1655.7e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "7cb69a6a7cb9825d"),
-    "fwd": (495.2e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "a0dd271e15f4b461"),
+    "bwd": (2010.8e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "eb91cd2bc157e042"),
+    "bwd_det": (1661.4e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "eb91cd2bc157e042"),
+    "fwd": (491.6e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "7535ee86c0921dac"),
 }
-TRAFFIC["bwd_det"] = TRAFFIC["bwd"]   # at d = 128 both entry points run the same kernels
 
 
 def measured_traffic(kernel, shape):

@@ -237,11 +237,6 @@ int bwd_common(const void *q, const void *k, const void *v, const void *o, const
     DeviceState *ds = nullptr;
     st = device_state(&ds);
     if (st != FA_OK) return st;
-    // At d = 128 the query-block dQ pass is faster than summing dQ with bulk reductions
-    // (measured on GB300: 2.58 vs 2.61 ms at B=2 H=32 N=8192 causal), so the default
-    // backward takes it too; at d = 64 the reductions are faster (0.20 vs 0.23 ms at
-    // B=4 H=16 N=2048).  fa_bwd_workspace_size covers both layouts.
-    if (d == 128) deterministic = true;
     BwdArgs a;
     std::memset(&a, 0, sizeof(a));
     const int BH = B * H, BHkv = B * Hkv;

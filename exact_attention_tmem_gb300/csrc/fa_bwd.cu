@@ -20,16 +20,17 @@
 //                 dV  += P^T dO_i           (A = P^T from TMEM)
 //                 dK  += dS^T Q_i           (A = dS^T from TMEM)
 //                 dQ_i = dS K_j             (A = dS from shared memory)
-//               dQ_i leaves tensor memory through a 32 KB shared staging tile and
-//               TMA bulk reduce-add (fp32) into the dQ accumulator; dK and dV
-//               accumulate in TMEM for the whole walk and are written once.
+//               dQ_i leaves tensor memory in 32-column boxes through a ring of two
+//               16 KB shared buffers (one box is written while the previous one is
+//               being reduced) and TMA bulk reduce-add (fp32) into the dQ accumulator;
+//               dK and dV accumulate in TMEM for the whole walk and are written once.
 //  3. bwd_post: dQ = bf16(scale * accumulator).
 //
 // Tensor memory (512 columns): dK [0, d) | dV [d, 2d) | S^T [2d, 2d+128) | dP^T [2d+128,
 // 2d+256).  P^T (bf16) is written over the first 64 S^T columns, dS^T over the first 64
-// dP^T columns, and dQ_i accumulates in the S^T columns once dV has consumed P^T.  Per
-// query block the MMA warp issues dV_i | dQ_i, dK_i | S^T_{i+1} (after the dQ_i read-out)
-// | dP^T_{i+1}: the read-out gates only the next S^T, not the next dP^T.
+// dP^T columns, and dQ_i accumulates in the dP^T columns once dK_i has consumed dS^T.
+// Per query block the MMA warp issues dK_i | dQ_i | dV_{i+1} | dP^T_{i+1} (after the dQ_i
+// read-out) | S^T_{i+2}: the read-out gates only the next dP^T.
 //
 // Warp roles (320 threads): warps 0-3 own one key row each (softmax recompute and dS),
 // warps 4-7 own one query row each (dQ read-out, staging and bulk reduce), warp 8
@@ -64,9 +65,8 @@ struct BwdCfg {
     static constexpr int kVecStages = 2;
     static constexpr int kVecBytes = kTileRows * 4;                 // 128 fp32
     static constexpr int kDSBytes = kDQ ? 2 * kBoxTileBytes : 0;    // 128 x 128 bf16
-    static constexpr int kDQHalfCols = 64;                          // fp32 columns per staging pass
-    static constexpr int kDQPasses = D / kDQHalfCols;
-    static constexpr int kDQStageBytes = kDQ ? kTileRows * kDQHalfCols * 4 : 0; // 32 KB = 2 boxes of 32 fp32
+    // dQ staging: a ring of two box buffers of 32 fp32 columns x 128 rows (16 KB each)
+    static constexpr int kDQStageBytes = kDQ ? 2 * kTileRows * 32 * 4 : 0;
     // shared memory map (offsets from a 1024-byte aligned base)
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kKOff + kTileBytes;
@@ -614,6 +614,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tDQr = tmem + lane_off + C::kDPCol;  // dQ_i accumulates in the dP^T columns
         bool ok = true;
+        int g = 0;   // dQ boxes issued so far
         for (int it = 0; kDQ && it < n_it; ++it) {
             const int i = q_block(it);
             // all 128 threads leave together, so none is left waiting at a named barrier
@@ -625,32 +626,27 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int ch = 0; ch < D / 32; ++ch) tmem_ld_x32(tDQr + 32u * ch, v[ch]);
             tc_fence_before();
             mbar_arrive(bar(B::kDQFree));
-            // Stage 64 fp32 columns at a time as two 128-byte-swizzled boxes of 32 columns
-            // (row r = 128 bytes per box) and add them into the accumulator with one TMA
-            // bulk reduction per box.  Rows past N fall outside the tensor map and are
-            // dropped by the reduction.
+            // dQ_i leaves in 32-column boxes (128 rows x 128 bytes, 128-byte swizzled)
+            // through a ring of two box buffers: box g is written while the bulk
+            // reduction of box g - 1 still reads the other buffer.  Rows past N fall
+            // outside the tensor map and are dropped by the reduction.
 #pragma unroll
-            for (int pass = 0; pass < C::kDQPasses; ++pass) {
-#pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    uint8_t *row = dQ_stage + b * C::kBoxTileBytes + r * kBoxBytes;
-                    const uint32_t(&src)[32] = v[2 * pass + b];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        *reinterpret_cast<uint4 *>(row + ((u ^ (r & 7)) << 4)) =
-                            make_uint4(src[4 * u], src[4 * u + 1], src[4 * u + 2], src[4 * u + 3]);
+            for (int b = 0; b < D / 32; ++b, ++g) {
+                if (g >= 2) {   // buffer g & 1 was last read by box g - 2
+                    if (threadIdx.x == 128) bulk_wait_group_read1();
+                    named_barrier_sync(1, 128);
                 }
+                uint8_t *row = dQ_stage + (g & 1) * C::kBoxTileBytes + r * kBoxBytes;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<uint4 *>(row + ((u ^ (r & 7)) << 4)) =
+                        make_uint4(v[b][4 * u], v[b][4 * u + 1], v[b][4 * u + 2], v[b][4 * u + 3]);
                 fence_proxy_async_smem();
                 named_barrier_sync(1, 128);
                 if (threadIdx.x == 128) {
-#pragma unroll
-                    for (int b = 0; b < 2; ++b)
-                        tma_reduce_add_3d(&tm_dq, sDQ + b * C::kBoxTileBytes, pass * C::kDQHalfCols + 32 * b,
-                                          i * kTileRows, q_head(it));
+                    tma_reduce_add_3d(&tm_dq, sDQ + (g & 1) * C::kBoxTileBytes, 32 * b, i * kTileRows, q_head(it));
                     bulk_commit_group();
-                    bulk_wait_group_read0();
                 }
-                named_barrier_sync(1, 128);
             }
         }
         if (threadIdx.x == 128) bulk_wait_group0();

@@ -109,12 +109,9 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   workspace   device buffer of at least fa_bwd_workspace_size(B,H,N,d)
  *               bytes, 256-byte aligned; its contents on entry do not matter
  *               and are scratch on exit
- * At d = 128 dQ is computed by a separate query-block pass that sums the key
- * blocks in a fixed order (the kernels of fa_bwd_deterministic, faster at this head
- * dimension), so every output is bit-identical from run to run.  At d = 64 the dQ
- * contributions of different key blocks are summed with fp32 bulk reductions in an
- * order that varies, so dq can differ from run to run in the last bits; dk and dv
- * are deterministic.
+ * The dQ contributions of different key blocks are summed with fp32 bulk
+ * reductions in an order that varies, so dq can differ from run to run in the last
+ * bits; dk and dv are deterministic.  fa_bwd_deterministic gives bit-identical dq.
  * Page: "FlashAttention" (deep dive), section "How it works" (backward
  * recomputes P = exp(Q K^T * scale - L), D = rowsum(dO o O),
  * dS = P o (dP - D)); the scale enters dQ and dK by the chain rule.

@@ -70,9 +70,9 @@ def test_bwd_large_scores():
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_bwd_dk_dv_deterministic_and_in_bounds(d):
-    """dK and dV involve no atomics: two runs agree bit for bit; at d = 128 dQ has one
-    writer per row too and agrees bit for bit, at d = 64 it is summed with reductions
-    whose order varies.  Sentinel padding around every gradient buffer is untouched."""
+    """dK and dV involve no atomics: two runs agree bit for bit; dQ is summed with
+    reductions whose order varies, so only its last bits may differ.  Sentinel padding
+    around every gradient buffer is untouched."""
     import exact_attention_tmem_gb300 as fa
     B, H, N = 2, 2, 300
     q, k, v, do = to_dev(*inputs.random_inputs(B, H, N, d, seed=45, with_grad_out=True))
@@ -85,8 +85,6 @@ def test_bwd_dk_dv_deterministic_and_in_bounds(d):
     fa.bwd(q, k, v, o, lse, do, causal=True, dq=grads[0], dk=grads[1], dv=grads[2])
     torch.cuda.synchronize()
     assert torch.equal(first[1], grads[1]) and torch.equal(first[2], grads[2])
-    if d == 128:
-        assert torch.equal(first[0], grads[0])
     assert float((first[0].float() - grads[0].float()).abs().max()) < 1e-2
     for b in bufs:
         assert bool((b[n:] == 3.0).all())

@@ -3,9 +3,8 @@ heads, against the same step on device tensors (fa_fwd then fa_bwd) and, on a sm
 case, against the fp64 oracle.
 
 Every head is an independent problem and the kernels compute each head the same way
-whatever the launch holds, so at d = 128 (where fa_bwd writes each dQ row once) every
-output must equal the device path bit for bit; at d = 64 dQ is summed with reductions
-whose order varies, so dQ is compared within a tolerance and the rest bit for bit."""
+whatever the launch holds, so o, lse, dk and dv must equal the device path bit for bit;
+dQ is summed with reductions whose order varies, so it is compared within a tolerance."""
 import math
 
 import pytest
@@ -54,7 +53,7 @@ def test_host_step_matches_device_step(d, causal, chunk):
     ref = device_step(q, k, v, do, causal, scale)
     got = host_step(q, k, v, do, causal, scale, chunk)
     for name, g, r in zip(("o", "lse", "dq", "dk", "dv"), got, ref):
-        if name == "dq" and d == 64:
+        if name == "dq":
             assert float((g.float() - r.float()).abs().max()) <= 1e-2 * float(r.float().abs().max())
         else:
             assert torch.equal(g, r), name
@@ -66,8 +65,11 @@ def test_host_step_pageable_memory():
     q, k, v, do = inputs.random_inputs(B, H, N, d, seed=62, with_grad_out=True)
     ref = device_step(q, k, v, do, True, 0.1)
     got = host_step(q, k, v, do, True, 0.1, chunk=2, pinned=False)
-    for g, r in zip(got, ref):
-        assert torch.equal(g, r)
+    for name, g, r in zip(("o", "lse", "dq", "dk", "dv"), got, ref):
+        if name == "dq":
+            assert float((g.float() - r.float()).abs().max()) <= 1e-2 * float(r.float().abs().max())
+        else:
+            assert torch.equal(g, r), name
 
 
 def test_host_step_against_oracle():
@@ -99,5 +101,8 @@ def test_host_step_waits_for_earlier_work_on_the_stream():
     hq.copy_(qd, non_blocking=True)        # q arrives in host memory only after that
     out = fa.fwd_bwd_host(hq, hk, hv, hdo, causal=False, scale=0.1, chunk_heads=1)
     torch.cuda.current_stream().synchronize()
-    for g, r in zip(out, ref):
-        assert torch.equal(g, r)
+    for name, g, r in zip(("o", "lse", "dq", "dk", "dv"), out, ref):
+        if name == "dq":
+            assert float((g.float() - r.float()).abs().max()) <= 1e-2 * float(r.float().abs().max())
+        else:
+            assert torch.equal(g, r), name
