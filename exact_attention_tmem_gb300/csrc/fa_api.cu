@@ -4,6 +4,7 @@
 // Every check that needs no GPU runs first, so that argument errors are reported
 // identically on a machine without one.  Nothing here allocates device memory
 // or synchronises a stream (fa_get_device_status excepted, by contract).
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -348,14 +349,34 @@ extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, f
     if (st != FA_OK) return st;
     const int max_chunks = decode_max_chunks(Nk);
     const int BHkv = B * Hkv;
+    const int stages = (Nk + kDecodeChunkAlign - 1) / kDecodeChunkAlign;
     int want = num_chunks;
-    if (want == 0) {  // enough CTAs for two per SM
-        const long long target = 2LL * (ds->sm_count > 0 ? ds->sm_count : 1);
-        want = static_cast<int>((target + BHkv - 1) / BHkv);
+    if (want == 0) {
+        // Fill every CTA slot and keep the last wave full.  A CTA's time is about its
+        // number of 64-key stages, so the kernel takes about waves x stages per chunk;
+        // take the chunk count (up to 8 x the fewest that fill the slots) that
+        // minimises it, the fewest chunks on a tie.
+        int per_sm = 2;
+        cudaError_t oe = decode_ctas_per_sm(d, H / Hkv, &per_sm);
+        if (oe != cudaSuccess) return cuda_fail(oe);
+        const long long slots = static_cast<long long>(per_sm > 0 ? per_sm : 1) * (ds->sm_count > 0 ? ds->sm_count : 1);
+        const long long units = static_cast<long long>(BHkv) * (H / Hkv / decode_subgroup(H / Hkv));
+        const long long w0 = std::min<long long>(std::max<long long>((slots + units - 1) / units, 1), max_chunks);
+        long long best_cost = LLONG_MAX;
+        for (long long w = w0; w <= std::min<long long>(8 * w0, max_chunks); ++w) {
+            const long long cs = (stages + w - 1) / w;
+            const long long n = (stages + cs - 1) / cs;
+            const long long ctas = static_cast<long long>(BHkv) * (H / Hkv / decode_subgroup(H / Hkv)) * n;
+            const long long waves = (ctas + slots - 1) / slots;
+            const long long cost = waves * cs;
+            if (cost < best_cost) {
+                best_cost = cost;
+                want = static_cast<int>(w);
+            }
+        }
     }
     if (want < 1) want = 1;
     if (want > max_chunks) want = max_chunks;
-    const int stages = (Nk + kDecodeChunkAlign - 1) / kDecodeChunkAlign;
     const int chunk_stages = (stages + want - 1) / want;
     DecodeArgs a;
     std::memset(&a, 0, sizeof(a));

@@ -18,8 +18,8 @@
 //                 S^T  = K_j Q_i^T          (TMEM)        -> P^T = 2^(S^T*scale*log2e - L2_i)
 //                 dP^T = V_j dO_i^T         (TMEM)        -> dS^T = P^T o (dP^T - D_i)
 //                 dV  += P^T dO_i           (A = P^T from TMEM)
-//                 dK  += dS^T Q_i           (A = dS^T from TMEM)
-//                 dQ_i = dS K_j             (A = dS from shared memory)
+//                 dQ_i = dS K_j             (A = dS from shared memory, MN-major)
+//                 dK  += dS^T Q_i           (A = the same tile, K-major)
 //               dQ_i leaves tensor memory in 32-column boxes through a ring of two
 //               16 KB shared buffers (one box is written while the previous one is
 //               being reduced) and TMA bulk reduce-add (fp32) into the dQ accumulator;
@@ -27,10 +27,10 @@
 //  3. bwd_post: dQ = bf16(scale * accumulator).
 //
 // Tensor memory (512 columns): dK [0, d) | dV [d, 2d) | S^T [2d, 2d+128) | dP^T [2d+128,
-// 2d+256).  P^T (bf16) is written over the first 64 S^T columns, dS^T over the first 64
-// dP^T columns, and dQ_i accumulates in the dP^T columns once dK_i has consumed dS^T.
-// Per query block the MMA warp issues dK_i | dQ_i | dV_{i+1} | dP^T_{i+1} (after the dQ_i
-// read-out) | S^T_{i+2}: the read-out gates only the next dP^T.
+// 2d+256).  P^T (bf16) is written over the first 64 S^T columns, and dQ_i accumulates in
+// the dP^T columns once the softmax warps have read dP^T.  Per query block the MMA warp
+// issues dQ_i | dK_i | dP^T_{i+1} (after the dQ_i read-out) | dV_{i+1} | S^T_{i+2}: the
+// read-out gates only the next dP^T.
 //
 // Warp roles (320 threads): warps 0-3 own one key row each (softmax recompute and dS),
 // warps 4-7 own one query row each (dQ read-out, staging and bulk reduce), warp 8
@@ -394,10 +394,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 umma_commit(bar(B::kDPFull));
             }
             if constexpr (kDQ) {
-                // dQ_i accumulates in the dP^T columns once dK_i has consumed dS^T from
-                // them.  Per query block: dK_i | dQ_i | dV_{i+1} | dP^T_{i+1} (after the
-                // dQ_i read-out) | S^T_{i+2}, so the read-out overlaps dV_{i+1} and the
-                // softmax warps compute P_{i+1} while dK_i and dQ_i run.
+                // dS_i is in shared memory only (the dS^T tile read K-major is dK's A
+                // operand, read MN-major it is dQ's), so dQ_i goes first, into the dP^T
+                // columns the softmax warps have finished reading.  Per query block:
+                // dQ_i | dK_i | dP^T_{i+1} (after the dQ_i read-out) | dV_{i+1} |
+                // S^T_{i+2}: the chain from dS_i to dS_{i+1} is dQ, dK, the read-out and
+                // dP^T; dK_i completes before dP^T_{i+1}, so the softmax warps overwrite
+                // the dS tile only after both products have read it.
                 if (ok) {  // dV_0, then S^T_1
                     ok = mbar_wait_w(bar(B::kPFull), 0, kSiteBMmaP);
                     if (ok) {
@@ -416,13 +419,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 for (int it = 0; ok && it < n_it; ++it) {
                     const int qs_it = it % C::kQStages;
-                    // dK += dS^T Q_i (dS^T from the dP^T columns), then dQ_i = dS K_j
-                    // (dS from shared memory) into the same columns
                     if (!mbar_wait_w(bar(B::kDSFull), it & 1, kSiteBMmaDS)) { ok = false; break; }
                     tc_fence_after();
-                    mma_tn(tDK, tDP, sQ + qs_it * C::kTileBytes, it > 0);
-                    umma_commit(bar(B::kQEmpty + qs_it));
-                    {
+                    {   // dQ_i = dS K_j (A = dS, MN-major) into the dP^T columns
                         const uint64_t a0 = sdesc_sw128(sDS, C::kBoxTileBytes, 1024);
                         const uint64_t b0 = sdesc_sw128(sK, C::kBoxTileBytes, 1024);
                         uint64_t a[C::kRowSteps], b[C::kRowSteps];
@@ -434,18 +433,32 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         umma_f16_ss_x8(tDP, a, b, C::kIdescDQ, 0u);
                     }
                     umma_commit(bar(B::kDQFull));
+                    {   // dK += dS^T Q_i (A = the same tile, K-major over the query rows)
+                        const uint64_t a0 = sdesc_sw128(sDS, 16, 1024);
+                        const uint64_t b0 = sdesc_sw128(sQ + qs_it * C::kTileBytes, C::kBoxTileBytes, 1024);
+                        uint64_t a[C::kRowSteps], b[C::kRowSteps];
+#pragma unroll
+                        for (int kk = 0; kk < C::kRowSteps; ++kk) {
+                            a[kk] = sdesc_step(a0, (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32);
+                            b[kk] = sdesc_step(b0, kk * 16 * kBoxBytes);
+                        }
+                        umma_f16_ss_x8(tDK, a, b, C::kIdescTS, it > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bar(B::kQEmpty + qs_it));
                     if (it + 1 < n_it) {
-                        // dV += P^T dO_{i+1} (P^T from the S^T columns)
-                        if (!mbar_wait_w(bar(B::kPFull), (it + 1) & 1, kSiteBMmaP)) { ok = false; break; }
-                        tc_fence_after();
                         const int dn = wait_do(it + 1);
                         if (dn < 0) { ok = false; break; }
-                        mma_tn(tDV, tS, sDO + dn * C::kTileBytes, true);
-                        // dP^T_{i+1} once dQ_i has left the dP^T columns
+                        // dP^T_{i+1} once dQ_i has left the dP^T columns; it goes ahead of
+                        // dV_{i+1}, so the softmax warps' P_{i+1} is off the path from dS_i
+                        // to dS_{i+1} (it overlaps dQ_i, dK_i and dP^T_{i+1})
                         if (!mbar_wait_w(bar(B::kDQFree), it & 1, kSiteBMmaDQ)) { ok = false; break; }
                         tc_fence_after();
                         mma_kk(tDP, sV, sDO + dn * C::kTileBytes);
                         umma_commit(bar(B::kDPFull));
+                        // dV += P^T dO_{i+1} (P^T from the S^T columns)
+                        if (!mbar_wait_w(bar(B::kPFull), (it + 1) & 1, kSiteBMmaP)) { ok = false; break; }
+                        tc_fence_after();
+                        mma_tn(tDV, tS, sDO + dn * C::kTileBytes, true);
                         umma_commit(bar(B::kDOEmpty + dn));
                         if (it + 2 < n_it) {  // S^T_{i+2}: P^T_{i+1} is read by dV_{i+1} first
                             const int qn = wait_q(it + 2);
@@ -559,7 +572,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     dk2[t] = pack_bf16(ds.x, ds.y);
                 }
                 // shared: query columns 32*ch .. 32*ch+31 = box (ch / 2), 16-byte chunks
-                // 4*(ch % 2) .. 4*(ch % 2)+3 of this key's row (only the dQ product reads it)
+                // 4*(ch % 2) .. 4*(ch % 2)+3 of this key's row (read by the dQ and dK products)
                 if constexpr (kDQ) {
                     uint8_t *box = ds_row0 + (ch >> 1) * C::kBoxTileBytes;
 #pragma unroll
@@ -569,9 +582,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
                     }
                 }
-                // tensor memory: dS^T packed over the first 64 dP^T columns (chunk ch
-                // writes columns 16ch.., all of which have been read by now)
-                asm volatile(
+                // tensor memory (the dK/dV-only kernel: dK reads dS^T from there): dS^T
+                // packed over the first 64 dP^T columns (chunk ch writes columns 16ch..,
+                // all of which have been read by now)
+                if constexpr (!kDQ) asm volatile(
                     "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
                     "%12, %13, %14, %15, %16};\n\t" ::"r"(tDPr + 16u * ch),
                     "r"(dk2[0]), "r"(dk2[1]), "r"(dk2[2]), "r"(dk2[3]), "r"(dk2[4]), "r"(dk2[5]),
@@ -580,8 +594,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     : "memory");
                 if (ch < 3) tmem_wait_ld_fence(rbuf[(ch + 1) & 1]);
             }
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            fence_proxy_async_smem();
+            if constexpr (!kDQ) asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            if constexpr (kDQ) fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B::kDSFull));
         }

@@ -18,6 +18,10 @@
 //     (16 bytes of the row per lane, so a warp reads whole 256-byte rows), reduces the
 //     dot products with shuffles, and keeps its own (m, l, acc) per query head; the
 //     rescale is applied once per stage (a block of keys), as in the forward kernel.
+//     With several query heads per key/value head the work per byte grows with the
+//     group, so the CTA has 8 warps (two CTAs per SM up to 4 heads per group) and the
+//     products and the output update run on packed pairs (fma.rn.f32x2): the stream
+//     of dependent shuffles, exponentials and FMAs needs the warps to hide latency.
 //     At the end the lane groups' triples are merged through shared memory and the
 //     CTA writes one partial triple per query head to the workspace.
 //  2. decode_combine_kernel: one CTA per (batch, query head) merges the chunks'
@@ -32,7 +36,7 @@
 namespace fa {
 namespace {
 
-constexpr int kDecThreads = 128;
+constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kDecStageKeys = 64;
 constexpr int kDecStages = 3;
@@ -40,7 +44,7 @@ constexpr float kDecLn2 = 0.6931471805599453f;
 
 enum : int { kSiteDecFull = 71, kSiteDecDrain = 72 };
 
-template <int D>
+template <int D, int G>
 struct DecCfg {
     static constexpr int kRowBytes = D * 2;
     static constexpr int kTileBytes = kDecStageKeys * kRowBytes;      // K or V of one stage
@@ -49,9 +53,14 @@ struct DecCfg {
     static constexpr int kKeysPerStep = 32 / kLanesPerKey;            // keys per warp per step
     static constexpr int kGroups = kDecWarps * kKeysPerStep;          // lane groups per CTA
     static constexpr int kSteps = kDecStageKeys / kGroups;            // keys per lane group per stage
-    static constexpr int kBarOff = kDecStages * kStageBytes;
+    static constexpr int kRingBytes = kDecStages * kStageBytes;
+    // the lane groups' (m, l, acc) triples, merged through shared memory after the loop
+    static constexpr int kMergeBytes = (2 * kGroups * G + kGroups * G * D) * 4;
+    static constexpr int kBarOff = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
     static constexpr int kMiscOff = kBarOff + 8 * kDecStages;
     static constexpr int kSmemBytes = kMiscOff + 16;
+    // two CTAs per SM (16 warps) while the registers allow it
+    static constexpr int kMinBlocks = G <= 4 ? 2 : 1;
     static_assert(kDecStageKeys % kGroups == 0, "whole steps per stage");
 };
 
@@ -62,12 +71,12 @@ __device__ __forceinline__ float2 bf2f(uint32_t x) {
 // Partials layout in the workspace, per (query head bh, chunk c): m[bh][c], l[bh][c],
 // acc[bh][c][D] (fp32; m in base-2 units).
 template <int D, int G>
-__global__ void __launch_bounds__(kDecThreads, 2)
+__global__ void __launch_bounds__(kDecThreads, DecCfg<D, G>::kMinBlocks)
 decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                     const __nv_bfloat16 *__restrict__ v, float *__restrict__ part_m, float *__restrict__ part_l,
                     float *__restrict__ part_acc, int Nk, int chunk_keys, int num_chunks, int max_chunks,
-                    float scale_log2, unsigned int *status) {
-    using C = DecCfg<D>;
+                    int group, float scale_log2, unsigned int *status) {
+    using C = DecCfg<D, G>;
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t base = smem_u32(smem);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff);
@@ -78,8 +87,14 @@ decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
     const int warp = tid >> 5, lane = tid & 31;
     const int grp = warp * C::kKeysPerStep + lane / C::kLanesPerKey;   // lane group in the CTA
     const int sl = lane % C::kLanesPerKey;                            // 16-byte column chunk
-    const int bkv = blockIdx.x / num_chunks;                          // batch * Hkv + kv head
-    const int c = blockIdx.x % num_chunks;
+    // The `group` query heads of a key/value head are split into group / G sub-groups
+    // of G heads; the CTAs of one chunk's sub-groups are adjacent in the launch order,
+    // so all but the first read the chunk's K and V from L2.
+    const int nsub = group / G;
+    const int sub = blockIdx.x % nsub;
+    const int c = (blockIdx.x / nsub) % num_chunks;
+    const int bkv = blockIdx.x / (nsub * num_chunks);                 // batch * Hkv + kv head
+    const int64_t qh0 = static_cast<int64_t>(bkv) * group + sub * G;  // first query head of the CTA
     const int key0 = c * chunk_keys;
     const int key1 = min(Nk, key0 + chunk_keys);
     const int n_tiles = (key1 - key0 + kDecStageKeys - 1) / kDecStageKeys;
@@ -105,26 +120,27 @@ decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
     if (tid == 0)
         for (; issued < kDecStages && issued < n_tiles; ++issued) issue(issued);
 
-    // this lane's 8 query elements of each head, pre-scaled into base-2 score units
-    float qf[G][8];
+    // this lane's 8 query elements of each head (as 4 pairs), pre-scaled into base-2
+    // score units; products and the output update run on packed pairs (fma.rn.f32x2)
+    float2 qf[G][4];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        const uint4 raw = *reinterpret_cast<const uint4 *>(q + (static_cast<int64_t>(bkv) * G + g) * D + sl * 8);
+        const uint4 raw = *reinterpret_cast<const uint4 *>(q + (qh0 + g) * D + sl * 8);
         const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float2 f = bf2f(w[e]);
-            qf[g][2 * e] = f.x * scale_log2;
-            qf[g][2 * e + 1] = f.y * scale_log2;
+            qf[g][e] = make_float2(f.x * scale_log2, f.y * scale_log2);
         }
     }
-    float m[G], l[G], acc[G][8];
+    float m[G], l[G];
+    float2 acc[G][4];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         m[g] = -INFINITY;
         l[g] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+        for (int e = 0; e < 4; ++e) acc[g][e] = make_float2(0.f, 0.f);
     }
 
     bool ok = true;
@@ -143,17 +159,13 @@ decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
         for (int st = 0; st < C::kSteps; ++st) {
             const int key = st * C::kGroups + grp;
             const uint4 raw = *reinterpret_cast<const uint4 *>(sk + key * C::kRowBytes + sl * 16);
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            const float2 kf[4] = {bf2f(raw.x), bf2f(raw.y), bf2f(raw.z), bf2f(raw.w)};
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float a = 0.f;
+                float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = bf2f(w[e]);
-                    a = fmaf(qf[g][2 * e], f.x, a);
-                    a = fmaf(qf[g][2 * e + 1], f.y, a);
-                }
-                sc[st][g] = a;
+                for (int e = 0; e < 4; ++e) a = fma2(qf[g][e], kf[e], a);
+                sc[st][g] = a.x + a.y;
             }
         }
 #pragma unroll
@@ -171,9 +183,10 @@ decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
                 if (st * C::kGroups + grp < n_keys) mx = fmaxf(mx, sc[st][g]);
             if (mx > m[g]) {   // m = -inf on the first keys: the factor is 0 and acc, l are 0
                 const float a = ex2(m[g] - mx);
+                const float2 a2 = make_float2(a, a);
                 l[g] *= a;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[g][e] *= a;
+                for (int e = 0; e < 4; ++e) acc[g][e] = mul2(acc[g][e], a2);
                 m[g] = mx;
             }
         }
@@ -182,17 +195,14 @@ decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
             const int key = st * C::kGroups + grp;
             if (key >= n_keys) continue;   // keys past the chunk: no contribution
             const uint4 raw = *reinterpret_cast<const uint4 *>(sv + key * C::kRowBytes + sl * 16);
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            const float2 vf[4] = {bf2f(raw.x), bf2f(raw.y), bf2f(raw.z), bf2f(raw.w)};
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float p = ex2(sc[st][g] - m[g]);
+                const float2 p2 = make_float2(p, p);
                 l[g] += p;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = bf2f(w[e]);
-                    acc[g][2 * e] = fmaf(p, f.x, acc[g][2 * e]);
-                    acc[g][2 * e + 1] = fmaf(p, f.y, acc[g][2 * e + 1]);
-                }
+                for (int e = 0; e < 4; ++e) acc[g][e] = fma2(p2, vf[e], acc[g][e]);
             }
         }
     }
@@ -221,7 +231,8 @@ decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ag[(grp * G + g) * D + sl * 8 + e] = acc[g][e];
+        for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<float2 *>(&ag[(grp * G + g) * D + sl * 8 + 2 * e]) = acc[g][e];
     __syncthreads();
     for (int idx = tid; idx < G * D; idx += kDecThreads) {
         const int g = idx / D, e = idx % D;
@@ -234,7 +245,7 @@ decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
             L = fmaf(lg[r * G + g], wgt, L);
             A = fmaf(ag[(r * G + g) * D + e], wgt, A);
         }
-        const int64_t slot = (static_cast<int64_t>(bkv) * G + g) * max_chunks + c;
+        const int64_t slot = (qh0 + g) * max_chunks + c;
         part_acc[slot * D + e] = A;
         if (e == 0) {
             part_m[slot] = M;
@@ -266,40 +277,70 @@ decode_combine_kernel(const float *__restrict__ part_m, const float *__restrict_
 
 template <int D, int G>
 cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
-    using C = DecCfg<D>;
+    using C = DecCfg<D, G>;
     auto kern = decode_split_kernel<D, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const long long blocks = static_cast<long long>(a.BHkv) * a.num_chunks;
+    const long long blocks = static_cast<long long>(a.BHkv) * (a.group / G) * a.num_chunks;
     if (blocks <= 0 || blocks > INT_MAX) return cudaErrorInvalidValue;
     const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     kern<<<static_cast<unsigned>(blocks), kDecThreads, C::kSmemBytes, stream>>>(
         static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.k),
         static_cast<const __nv_bfloat16 *>(a.v), a.part_m, a.part_l, a.part_acc, a.Nk, a.chunk_keys, a.num_chunks,
-        a.max_chunks, scale_log2, a.status);
+        a.max_chunks, a.group, scale_log2, a.status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<D><<<static_cast<unsigned>(a.BHkv * G), D, 0, stream>>>(
+    decode_combine_kernel<D><<<static_cast<unsigned>(a.BHkv * a.group), D, 0, stream>>>(
         a.part_m, a.part_l, a.part_acc, static_cast<__nv_bfloat16 *>(a.o), a.lse, a.num_chunks, a.max_chunks);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
-    switch (a.group) {
+    switch (decode_subgroup(a.group)) {   // 1..5 or 7
         case 1: return launch_decode_t<D, 1>(a, stream);
         case 2: return launch_decode_t<D, 2>(a, stream);
         case 3: return launch_decode_t<D, 3>(a, stream);
         case 4: return launch_decode_t<D, 4>(a, stream);
         case 5: return launch_decode_t<D, 5>(a, stream);
-        case 6: return launch_decode_t<D, 6>(a, stream);
         case 7: return launch_decode_t<D, 7>(a, stream);
-        case 8: return launch_decode_t<D, 8>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int D>
+cudaError_t decode_ctas_per_sm_d(int group, int *out) {
+    group = decode_subgroup(group);
+    auto q = [out](auto kern, int smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kern, kDecThreads, smem);
+    };
+    switch (group) {
+        case 1: return q(decode_split_kernel<D, 1>, DecCfg<D, 1>::kSmemBytes);
+        case 2: return q(decode_split_kernel<D, 2>, DecCfg<D, 2>::kSmemBytes);
+        case 3: return q(decode_split_kernel<D, 3>, DecCfg<D, 3>::kSmemBytes);
+        case 4: return q(decode_split_kernel<D, 4>, DecCfg<D, 4>::kSmemBytes);
+        case 5: return q(decode_split_kernel<D, 5>, DecCfg<D, 5>::kSmemBytes);
+        case 7: return q(decode_split_kernel<D, 7>, DecCfg<D, 7>::kSmemBytes);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
+
+int decode_subgroup(int group) {
+    if (group <= 4) return group;
+    if (group % 4 == 0) return 4;
+    if (group % 3 == 0) return 3;
+    return group;
+}
+
+cudaError_t decode_ctas_per_sm(int d, int group, int *out) {
+    if (d == 64) return decode_ctas_per_sm_d<64>(group, out);
+    if (d == 128) return decode_ctas_per_sm_d<128>(group, out);
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t stream) {
     if (a.d == 64) return launch_decode_d<64>(a, stream);

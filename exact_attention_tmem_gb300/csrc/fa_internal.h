@@ -71,6 +71,11 @@ cudaError_t launch_fwd_bf16(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_bwd_bf16(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t stream);
+// Query heads per CTA of the decoding kernel for a group of `group` query heads per
+// key/value head (groups above 4 are split when 4 or 3 divides them), and the CTAs of
+// that kernel resident per SM (occupancy).
+int decode_subgroup(int group);
+cudaError_t decode_ctas_per_sm(int d, int group, int *out);
 cudaError_t launch_fwd_fp8(const Fp8FwdArgs &a, cudaStream_t stream);
 // descale doubles as the per-head amax scratch while the kernels run
 cudaError_t launch_quantize_qk_fp8(const void *x, const float *signs, void *x8, float *descale, int BH, int N,
