@@ -124,14 +124,15 @@ int get_encoder(EncodeTiledFn *fn) {
 
 // [BH, N, d] viewed as 3-D: d innermost, then N, then BH.  One box is 128 bytes of a
 // row by 128 rows, 128-byte swizzled (the layout the MMA descriptors expect).
-int make_tmap(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int eb, int d, int N, int BH) {
+int make_tmap(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int eb, int d, int N, int BH,
+              int rows = kTileRows) {
     EncodeTiledFn enc;
     int st = get_encoder(&enc);
     if (st != FA_OK) return st;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * eb, static_cast<cuuint64_t>(d) * eb * N};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBoxBytes / eb), static_cast<cuuint32_t>(kTileRows), 1};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBoxBytes / eb), static_cast<cuuint32_t>(rows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -316,7 +317,7 @@ int decode_max_chunks(int Nk) {
 int check_decode(int B, int H, int Hkv, int Nk, int d) {
     int st = check_shape(B, H, Nk, d, Hkv);
     if (st != FA_OK) return st;
-    if (H / Hkv > 8) return FA_ERR_UNSUPPORTED;
+    if (H / Hkv > kDecodeMaxGroup) return FA_ERR_UNSUPPORTED;
     return FA_OK;
 }
 
@@ -380,6 +381,10 @@ extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, f
     const int chunk_stages = (stages + want - 1) / want;
     DecodeArgs a;
     std::memset(&a, 0, sizeof(a));
+    if ((st = make_tmap(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, Nk, BHkv, kDecodeBoxRows)) != FA_OK)
+        return st;
+    if ((st = make_tmap(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, Nk, BHkv, kDecodeBoxRows)) != FA_OK)
+        return st;
     a.q = q;
     a.k = k;
     a.v = v;

@@ -254,6 +254,258 @@ decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
     }
 }
 
+// ------------------------------------------------------------------------------------
+// Tensor-core variant for groups of query heads (grouped-query attention).  With G query
+// heads per key/value head every K and V element feeds G dot products, which on the CUDA
+// cores costs more issue slots than the memory stream allows once G reaches a few heads.
+// Here the G query rows (padded to 16) are the M dimension of mma.sync m16n8k16 (bf16
+// in, fp32 accumulate):
+//   S (16 x 16 keys) = Q (16 x d) K^T      B fragments of K read with ldmatrix
+//   O (16 x d)      += P (16 x 16 keys) V  P = the S accumulator fragment repacked as the
+//                                          A fragment; V read with ldmatrix.trans
+// One CTA of 4 warps per (batch, key/value head, chunk); a stage holds 64 keys (K and V,
+// loaded by TMA with 128-byte swizzle so that the ldmatrix rows hit distinct banks) and
+// each warp takes 16 of them, keeping its own (m, l, O) per query row; the warps' triples
+// are merged through shared memory into one partial triple per query head and chunk,
+// the layout decode_combine_kernel merges.
+constexpr int kMmaDecThreads = 128;
+constexpr int kMmaDecStages = 3;
+
+template <int D>
+struct DecMmaCfg {
+    static constexpr int kBoxes = D * 2 / 128;                   // 128-byte boxes per row
+    static constexpr int kBoxBytes = kDecodeBoxRows * 128;       // 64 keys x 128 bytes
+    static constexpr int kTileBytes = kBoxes * kBoxBytes;        // K or V of one stage
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kRingBytes = kMmaDecStages * kStageBytes;
+    static constexpr int kMergeBytes = 4 * (2 * 16 + 16 * D) * 4;    // per warp: m, l, O (16 rows)
+    static constexpr int kBarOff = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+    static constexpr int kMiscOff = kBarOff + 8 * kMmaDecStages;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;      // + room to align the base to 1 KB
+    static_assert(kDecodeBoxRows == 4 * 16, "four warps of 16 keys per stage");
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kMmaDecThreads, 2)
+decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __nv_bfloat16 *__restrict__ q, float *__restrict__ part_m, float *__restrict__ part_l,
+                  float *__restrict__ part_acc, int Nk, int chunk_keys, int num_chunks, int max_chunks, int group,
+                  float scale_log2, unsigned int *status) {
+    using C = DecMmaCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;     // 128-byte swizzle repeats every 1 KB
+    uint8_t *smem = smem_raw + (base - raw);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff);
+    const WaitCtx wc{abort_flag, status};
+    auto full_bar = [&](int s) -> uint32_t { return base + C::kBarOff + 8u * static_cast<uint32_t>(s); };
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int bkv = blockIdx.x / num_chunks;          // batch * Hkv + key/value head
+    const int c = blockIdx.x % num_chunks;
+    const int key0 = c * chunk_keys;
+    const int key1 = min(Nk, key0 + chunk_keys);
+    const int n_tiles = (key1 - key0 + kDecodeBoxRows - 1) / kDecodeBoxRows;
+
+    if (tid == 0) {
+        for (int s = 0; s < kMmaDecStages; ++s) mbar_init(full_bar(s), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto issue = [&](int t) {
+        const int s = t % kMmaDecStages;
+        const uint32_t dst = base + s * C::kStageBytes;
+        mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);   // rows past Nk arrive zero-filled
+        for (int b = 0; b < C::kBoxes; ++b) {
+            tma_load_3d(dst + b * C::kBoxBytes, &tm_k, full_bar(s), b * 64, key0 + t * kDecodeBoxRows, bkv);
+            tma_load_3d(dst + C::kTileBytes + b * C::kBoxBytes, &tm_v, full_bar(s), b * 64,
+                        key0 + t * kDecodeBoxRows, bkv);
+        }
+    };
+    int issued = 0;
+    if (tid == 0) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        for (; issued < kMmaDecStages && issued < n_tiles; ++issued) issue(issued);
+    }
+
+    // Q fragments: rows g0 = lane / 4 and g1 = g0 + 8 of the group (zero past it),
+    // columns 16k + 2(lane % 4) (+1, +8, +9)
+    const int g0 = lane >> 2, g1 = g0 + 8;
+    const int cc = 2 * (lane & 3);
+    auto q2 = [&](int g, int col) -> uint32_t {
+        if (g >= group) return 0u;
+        return *reinterpret_cast<const uint32_t *>(q + (static_cast<int64_t>(bkv) * group + g) * D + col);
+    };
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+        qa[k][0] = q2(g0, 16 * k + cc);
+        qa[k][1] = q2(g1, 16 * k + cc);
+        qa[k][2] = q2(g0, 16 * k + cc + 8);
+        qa[k][3] = q2(g1, 16 * k + cc + 8);
+    }
+    float o[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY;   // running max of rows g0, g1 (base-2 units)
+    float l0 = 0.f, l1 = 0.f;               // this thread's part of the running sums
+    // a 16-byte chunk `ch` (8 elements of d) of stage row `key` in a swizzled tile
+    auto chunk_addr = [&](uint32_t tile, int key, int ch) -> uint32_t {
+        return tile + (ch >> 3) * C::kBoxBytes + key * 128 + (((ch & 7) ^ (key & 7)) << 4);
+    };
+    const int kw = 16 * warp;               // this warp's keys in a stage
+
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % kMmaDecStages;
+        ok = __syncthreads_and(mbar_wait(full_bar(s), (t / kMmaDecStages) & 1, wc, kSiteDecFull)) != 0;
+        if (!ok) break;
+        // every thread is past tile t - 1: its stage can be refilled
+        if (tid == 0 && t >= 1 && issued < n_tiles) issue(issued++);
+        const uint32_t sk = base + s * C::kStageBytes, sv = sk + C::kTileBytes;
+        const int n_keys = min(kDecodeBoxRows, key1 - (key0 + t * kDecodeBoxRows));
+        // S = Q K^T over this warp's 16 keys (two 8-key column tiles)
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const int key = kw + 8 * n + (lane & 7);
+#pragma unroll
+            for (int kp = 0; kp < D / 32; ++kp) {
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4(chunk_addr(sk, key, 4 * kp + (lane >> 3)), r0, r1, r2, r3);
+                mma_bf16_16816(sc[n], qa[2 * kp], r0, r1);
+                mma_bf16_16816(sc[n], qa[2 * kp + 1], r2, r3);
+            }
+        }
+        // scaled scores, keys past the chunk masked; online softmax per row
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const bool valid = kw + 8 * n + cc + e < n_keys;
+                sc[n][e] = valid ? sc[n][e] * scale_log2 : -INFINITY;
+                sc[n][2 + e] = valid ? sc[n][2 + e] * scale_log2 : -INFINITY;
+                mx0 = fmaxf(mx0, sc[n][e]);
+                mx1 = fmaxf(mx1, sc[n][2 + e]);
+            }
+#pragma unroll
+        for (int off = 1; off <= 2; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        // a row that has seen no key yet keeps m = -inf, l = 0, O = 0
+        const float a0 = mn0 == -INFINITY ? 1.f : ex2(m0 - mn0);
+        const float a1 = mn1 == -INFINITY ? 1.f : ex2(m1 - mn1);
+        const float base0 = mn0 == -INFINITY ? 0.f : mn0, base1 = mn1 == -INFINITY ? 0.f : mn1;
+        m0 = mn0;
+        m1 = mn1;
+        float p[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                p[n][e] = ex2(sc[n][e] - base0);
+                p[n][2 + e] = ex2(sc[n][2 + e] - base1);
+            }
+        l0 = l0 * a0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+        l1 = l1 * a1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+        if (a0 != 1.f || a1 != 1.f) {
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+                o[n][0] *= a0;
+                o[n][1] *= a0;
+                o[n][2] *= a1;
+                o[n][3] *= a1;
+            }
+        }
+        // P as the A fragment (rows g0, g1; keys cc, cc + 1, cc + 8, cc + 9 of the 16)
+        const uint32_t pa[4] = {pack_bf16(p[0][0], p[0][1]), pack_bf16(p[0][2], p[0][3]),
+                                pack_bf16(p[1][0], p[1][1]), pack_bf16(p[1][2], p[1][3])};
+        // O += P V: V read transposed, two 8-column tiles of d per ldmatrix
+#pragma unroll
+        for (int np = 0; np < D / 16; ++np) {
+            const int key = kw + 8 * ((lane >> 3) & 1) + (lane & 7);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_t(chunk_addr(sv, key, 2 * np + (lane >> 4)), r0, r1, r2, r3);
+            mma_bf16_16816(o[2 * np], pa, r0, r1);
+            mma_bf16_16816(o[2 * np + 1], pa, r2, r3);
+        }
+    }
+    if (!ok) {
+        // every copy issued must land before the CTA exits
+        if (tid == 0)
+            for (int s = 0; s < kMmaDecStages && s < issued; ++s) {
+                const int last = s + ((issued - 1 - s) / kMmaDecStages) * kMmaDecStages;
+                mbar_wait_drain(full_bar(s), (last / kMmaDecStages) & 1, wc, kSiteDecDrain);
+            }
+        return;
+    }
+
+    // ---- merge the four warps' triples through shared memory (the ring is idle now)
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    __syncthreads();
+    float *mw = reinterpret_cast<float *>(smem);        // [4][16]
+    float *lw = mw + 4 * 16;                            // [4][16]
+    float *ow = lw + 4 * 16;                            // [4][16][D]
+    if ((lane & 3) == 0) {
+        mw[warp * 16 + g0] = m0;
+        mw[warp * 16 + g1] = m1;
+        lw[warp * 16 + g0] = l0;
+        lw[warp * 16 + g1] = l1;
+    }
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+        *reinterpret_cast<float2 *>(&ow[(warp * 16 + g0) * D + 8 * n + cc]) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2 *>(&ow[(warp * 16 + g1) * D + 8 * n + cc]) = make_float2(o[n][2], o[n][3]);
+    }
+    __syncthreads();
+    for (int idx = tid; idx < group * D; idx += kMmaDecThreads) {
+        const int g = idx / D, e = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, mw[w * 16 + g]);
+        float L = 0.f, A = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float mr = mw[w * 16 + g];
+            const float wgt = mr == -INFINITY ? 0.f : ex2(mr - M);   // warps that saw no key weigh 0
+            L = fmaf(lw[w * 16 + g], wgt, L);
+            A = fmaf(ow[(w * 16 + g) * D + e], wgt, A);
+        }
+        const int64_t slot = (static_cast<int64_t>(bkv) * group + g) * max_chunks + c;
+        part_acc[slot * D + e] = A;
+        if (e == 0) {
+            part_m[slot] = M;
+            part_l[slot] = L;
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(D)
 decode_combine_kernel(const float *__restrict__ part_m, const float *__restrict__ part_l,
@@ -296,7 +548,27 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
 }
 
 template <int D>
+cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t stream) {
+    using C = DecMmaCfg<D>;
+    auto kern = decode_mma_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const long long blocks = static_cast<long long>(a.BHkv) * a.num_chunks;
+    if (blocks <= 0 || blocks > INT_MAX) return cudaErrorInvalidValue;
+    const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+    kern<<<static_cast<unsigned>(blocks), kMmaDecThreads, C::kSmemBytes, stream>>>(
+        a.tm_k, a.tm_v, static_cast<const __nv_bfloat16 *>(a.q), a.part_m, a.part_l, a.part_acc, a.Nk,
+        a.chunk_keys, a.num_chunks, a.max_chunks, a.group, scale_log2, a.status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_combine_kernel<D><<<static_cast<unsigned>(a.BHkv * a.group), D, 0, stream>>>(
+        a.part_m, a.part_l, a.part_acc, static_cast<__nv_bfloat16 *>(a.o), a.lse, a.num_chunks, a.max_chunks);
+    return cudaGetLastError();
+}
+
+template <int D>
 cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
+    if (a.group >= kDecodeMmaMinGroup) return launch_decode_mma<D>(a, stream);
     switch (decode_subgroup(a.group)) {   // 1..5 or 7
         case 1: return launch_decode_t<D, 1>(a, stream);
         case 2: return launch_decode_t<D, 2>(a, stream);
@@ -310,6 +582,13 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
 
 template <int D>
 cudaError_t decode_ctas_per_sm_d(int group, int *out) {
+    if (group >= kDecodeMmaMinGroup) {
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             DecMmaCfg<D>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, decode_mma_kernel<D>, kMmaDecThreads,
+                                                             DecMmaCfg<D>::kSmemBytes);
+    }
     group = decode_subgroup(group);
     auto q = [out](auto kern, int smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -330,6 +609,7 @@ cudaError_t decode_ctas_per_sm_d(int group, int *out) {
 }  // namespace
 
 int decode_subgroup(int group) {
+    if (group >= kDecodeMmaMinGroup) return group;   // the tensor-core kernel takes the whole group
     if (group <= 4) return group;
     if (group % 4 == 0) return 4;
     if (group % 3 == 0) return 3;

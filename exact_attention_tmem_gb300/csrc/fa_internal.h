@@ -39,10 +39,15 @@ struct BwdArgs {
     unsigned int *status;
 };
 
+constexpr int kDecodeBoxRows = 64;    // keys per stage of the tensor-core decoding kernel
+constexpr int kDecodeMmaMinGroup = 2; // query heads per key/value head from which decoding uses it
+constexpr int kDecodeMaxGroup = 16;   // the tensor-core kernel's M dimension
+
 // Decoding: one query row per head ([B*H, d]) against K, V [B*Hkv, Nk, d]; the keys of
 // each key/value head are split into num_chunks chunks of chunk_keys keys (a multiple
 // of 64), whose partial (m, l, acc) triples land in the workspace before the merge.
 struct DecodeArgs {
+    CUtensorMap tm_k, tm_v;   // [B*Hkv, Nk, d] with 64-row boxes (the tensor-core kernel)
     const void *q, *k, *v;
     void *o;
     float *lse;

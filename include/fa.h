@@ -168,16 +168,17 @@ size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nk, int d);
  * Decoding: one query row per head against a long key/value sequence, the keys
  * split into chunks processed in parallel and merged.
  *   q          [B,H,d]       bf16, read only: the newest position's query per head
- *   k, v       [B,Hkv,Nk,d]  bf16, read only; Hkv divides H, H / Hkv <= 8; query
+ *   k, v       [B,Hkv,Nk,d]  bf16, read only; Hkv divides H, H / Hkv <= 16; query
  *                            head h uses key/value head h / (H / Hkv)
  *   o          [B,H,d]       bf16, written: softmax(scale * q k^T) v (every key visible)
  *   lse        [B,H]         fp32, written: natural-log logsumexp of the scaled scores
  *   workspace  device buffer of at least fa_decode_workspace_size(B,H,Hkv,Nk,d)
  *              bytes, 256-byte aligned; scratch
- *   num_chunks chunks per key/value head: 0 lets the library choose (about two
- *              CTAs per SM), otherwise it is clamped to [1, min(ceil(Nk/64), 256)];
+ *   num_chunks chunks per key/value head: 0 lets the library choose (every CTA
+ *              slot filled, the last wave of CTAs full), otherwise it is clamped to
+ *              [1, min(ceil(Nk/64), 256)];
  *              chunks are whole multiples of 64 keys
- * d = 64 or 128.  Status codes as for fa_fwd; FA_ERR_UNSUPPORTED when H / Hkv > 8.
+ * d = 64 or 128.  Status codes as for fa_fwd; FA_ERR_UNSUPPORTED when H / Hkv > 16.
  * The result does not depend on num_chunks beyond fp32 rounding order.
  * Page: "FlashAttention" (deep dive), section "Implementation notes" (decoding with
  * one query row: parallelise over chunks of the keys and merge the partial

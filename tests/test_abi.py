@@ -225,7 +225,8 @@ def test_decode_workspace_size(lib):
     big = lib.fa_decode_workspace_size(1, 1, 1, 1 << 20, 64)   # capped at 256 chunks
     assert big == 2 * 1024 + 256 * 64 * 4
     assert lib.fa_decode_workspace_size(1, 4, 3, 100, 128) == 0      # Hkv does not divide H
-    assert lib.fa_decode_workspace_size(1, 18, 2, 100, 128) == 0     # group of 9
+    assert lib.fa_decode_workspace_size(1, 34, 2, 100, 128) == 0     # group of 17
+    assert lib.fa_decode_workspace_size(1, 32, 2, 100, 128) > 0      # group of 16
     assert lib.fa_decode_workspace_size(1, 4, 2, 100, 96) == 0
 
 
@@ -243,7 +244,7 @@ def test_decode_host_checks(lib):
     assert dec(lib, ws=W + 64) == _lib.FA_ERR_ALIGNMENT
     assert dec(lib, ptrs=[A, A, A + 8, A, A]) == _lib.FA_ERR_ALIGNMENT
     assert dec(lib, Hkv=3) == _lib.FA_ERR_INVALID_ARG
-    assert dec(lib, H=18, Hkv=2) == _lib.FA_ERR_UNSUPPORTED
+    assert dec(lib, H=34, Hkv=2) == _lib.FA_ERR_UNSUPPORTED
     assert dec(lib, d=96) == _lib.FA_ERR_UNSUPPORTED
     assert dec(lib, Nk=0) == _lib.FA_ERR_INVALID_ARG
     assert dec(lib, scale=float("nan")) == _lib.FA_ERR_INVALID_ARG

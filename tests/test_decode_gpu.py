@@ -47,6 +47,8 @@ CASES = [  # B, H, Hkv, Nk, d
     (1, 1, 1, 1, 64), (1, 2, 2, 1, 128), (2, 4, 4, 17, 128), (1, 8, 2, 63, 64), (2, 8, 1, 64, 128),
     (1, 4, 4, 65, 64), (2, 6, 2, 1000, 128), (1, 16, 2, 4097, 128), (3, 5, 5, 2500, 64),
     (1, 7, 1, 777, 128), (2, 32, 8, 8192, 128),
+    # larger groups (tensor-core kernel): 3, 9, 12, 16 query heads per key/value head
+    (2, 12, 4, 2048, 64), (1, 9, 1, 130, 128), (2, 24, 2, 1100, 128), (1, 16, 1, 300, 64), (1, 32, 2, 5000, 128),
 ]
 
 
