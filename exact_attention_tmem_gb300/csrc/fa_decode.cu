@@ -515,8 +515,11 @@ decode_combine_kernel(const float *__restrict__ part_m, const float *__restrict_
     const int e = threadIdx.x;
     const int64_t base = static_cast<int64_t>(bh) * max_chunks;
     float M = -INFINITY;
+#pragma unroll 8
     for (int c = 0; c < num_chunks; ++c) M = fmaxf(M, part_m[base + c]);
     float L = 0.f, A = 0.f;
+    // unrolled so that the chunks' loads are in flight together
+#pragma unroll 8
     for (int c = 0; c < num_chunks; ++c) {
         const float mc = part_m[base + c];
         const float wgt = mc == -INFINITY ? 0.f : ex2(mc - M);
