@@ -49,6 +49,7 @@ CASES = [  # B, H, Hkv, Nk, d
     (1, 7, 1, 777, 128), (2, 32, 8, 8192, 128),
     # larger groups (tensor-core kernel): 3, 9, 12, 16 query heads per key/value head
     (2, 12, 4, 2048, 64), (1, 9, 1, 130, 128), (2, 24, 2, 1100, 128), (1, 16, 1, 300, 64), (1, 32, 2, 5000, 128),
+    (1, 4, 1, 1, 128), (2, 4, 2, 65, 64), (1, 16, 1, 64, 128),   # one key, a ragged stage, one full stage
 ]
 
 
