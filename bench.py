@@ -43,9 +43,9 @@ REF_STEP_ROWS = 32      # query rows per head per step of the reference arm
 # they had when the counters were taken; after any change it reads as null until the
 # capture is repeated.
 TRAFFIC = {
-    "bwd": (2016.2e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "6def341c85fa7f83"),
-    "bwd_det": (1660.0e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "6def341c85fa7f83"),
-    "fwd": (491.4e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "2c796a86e4e380ed"),
+    "bwd": (2016.2e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "44e2e97555ae2ac6"),
+    "bwd_det": (1660.0e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "44e2e97555ae2ac6"),
+    "fwd": (491.4e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "0c0439e89c78474f"),
 }
 
 

@@ -90,7 +90,6 @@ struct BwdCfg {
     static constexpr int kRowSteps = kTileRows / 16; // K steps over 128 rows
     static constexpr uint32_t kIdescSS = make_idesc(kFormatBF16, 128, 128, false, false);
     static constexpr uint32_t kIdescTS = make_idesc(kFormatBF16, 128, D, false, true);
-    static constexpr uint32_t kIdescDQ = make_idesc(kFormatBF16, 128, D, true, true);
 
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert(2 * D + 256 <= 512, "tensor memory budget");
@@ -430,7 +429,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             a[kk] = sdesc_step(a0, kk * 16 * kBoxBytes);
                             b[kk] = sdesc_step(b0, kk * 16 * kBoxBytes);
                         }
-                        umma_f16_ss_x8(tDP, a, b, C::kIdescDQ, 0u);
+                        // A (dS) and B (K_j) both MN-major
+                        constexpr uint32_t kIdescDQ = make_idesc(kFormatBF16, 128, D, true, true);
+                        umma_f16_ss_x8(tDP, a, b, kIdescDQ, 0u);
                     }
                     umma_commit(bar(B::kDQFull));
                     {   // dK += dS^T Q_i (A = the same tile, K-major over the query rows)

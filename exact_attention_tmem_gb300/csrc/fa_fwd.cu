@@ -46,7 +46,6 @@ struct FwdCfg {
     // QT query tiles of 128 rows per CTA: 4 softmax warps per tile, then the MMA warp
     // and the TMA warp.  With QT = 1 two CTAs share an SM (half the shared memory and
     // tensor memory each); with QT = 2 one CTA owns the SM.
-    static constexpr int kQT = QT;
     static constexpr int kMmaWarp = 4 * QT;
     static constexpr int kLoadWarp = 4 * QT + 1;
     static constexpr int kThreads = 32 * (4 * QT + 2);
