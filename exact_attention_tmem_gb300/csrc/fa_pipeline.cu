@@ -6,14 +6,18 @@
 // section "How it works": Q, K, V of one head in, O and L of that head out, no state
 // between calls), so the B*H heads are cut into chunks of consecutive heads and each
 // chunk goes through three stages:
-//   copy-in  stream: q, k, v, dO of chunk c           host -> slot c % kSlots
-//   compute  stream: fa_fwd, then fa_bwd on the slot  (waits for copy-in of c); even
-//                    chunks run on the caller's stream, odd ones on an internal stream
-//   copy-out stream: o, lse, dq, dk, dv of chunk c    slot -> host (waits for c's kernels)
+//   copy-in  stream: q, k, v, then dO of chunk c      host -> slot c % kSlots
+//   compute  stream: fa_fwd once q, k, v have landed, fa_bwd once dO has; even chunks
+//                    run on the caller's stream, odd ones on an internal stream
+//   copy-out stream: o, lse of chunk c once its forward is done, then dq, dk, dv once
+//                    its backward is                  slot -> host
 // The copy-in of chunk c waits until the copy-out of chunk c - kSlots has drained the
 // slot it reuses.  With three slots the copies of chunks c + 1 and c - 1 run while the
 // kernels of chunk c do, and the kernels of two consecutive chunks may share the GPU
-// where one leaves SMs idle (the tail of a launch).  The device buffer (the slots)
+// where one leaves SMs idle (the tail of a launch).  Splitting each chunk's copies at
+// the forward/backward boundary lets the forward start before dO has landed and o, L
+// leave before the backward ends, which shortens the parts of the step (the first
+// copy-in, the last copy-out) that nothing overlaps.  The device buffer (the slots)
 // belongs to the caller; the internal streams and the events are created once per
 // device and reused.
 #include <climits>
@@ -63,7 +67,8 @@ struct PipeState {
     bool ready = false;
     cudaStream_t copy_in = nullptr, copy_out = nullptr, compute = nullptr;
     cudaEvent_t start = nullptr, done = nullptr;
-    cudaEvent_t h2d[kSlots] = {}, comp[kSlots] = {}, d2h[kSlots] = {};
+    // per slot: q, k, v landed | dO landed | forward done | backward done | outputs copied
+    cudaEvent_t h2d_fwd[kSlots] = {}, h2d_bwd[kSlots] = {}, fwd[kSlots] = {}, comp[kSlots] = {}, d2h[kSlots] = {};
 };
 PipeState g_pipe[kMaxDevices];
 std::mutex g_pipe_mu;   // held for the whole enqueue: the events are shared per device
@@ -82,16 +87,17 @@ int pipe_state(PipeState **out, int *cuda_err) {
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.start, ev_flags);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.done, ev_flags);
         for (int i = 0; i < kSlots && e == cudaSuccess; ++i) {
-            e = cudaEventCreateWithFlags(&s.h2d[i], ev_flags);
+            e = cudaEventCreateWithFlags(&s.h2d_fwd[i], ev_flags);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.h2d_bwd[i], ev_flags);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fwd[i], ev_flags);
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.comp[i], ev_flags);
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.d2h[i], ev_flags);
         }
         if (e != cudaSuccess) {   // release what was created; the next call starts over
             *cuda_err = e;
             for (int i = 0; i < kSlots; ++i) {
-                if (s.h2d[i]) cudaEventDestroy(s.h2d[i]);
-                if (s.comp[i]) cudaEventDestroy(s.comp[i]);
-                if (s.d2h[i]) cudaEventDestroy(s.d2h[i]);
+                for (cudaEvent_t ev : {s.h2d_fwd[i], s.h2d_bwd[i], s.fwd[i], s.comp[i], s.d2h[i]})
+                    if (ev) cudaEventDestroy(ev);
             }
             if (s.start) cudaEventDestroy(s.start);
             if (s.done) cudaEventDestroy(s.done);
@@ -162,37 +168,44 @@ extern "C" int fa_fwd_bwd_host(const void *q, const void *k, const void *v, cons
         for (int i = 0; i < 8; ++i) t[i] = slot + L.tensor_off(i);   // q k v dO o dq dk dv
         float *lse_d = reinterpret_cast<float *>(slot + L.lse_off());
         void *ws = slot + L.ws_off();
-        const size_t bytes = n * head_bytes, off = h0 * head_bytes;
-        // copy-in: the slot is free once the copy-out of chunk c - kSlots has read it
+        const size_t bytes = static_cast<size_t>(n) * head_bytes, off = static_cast<size_t>(h0) * head_bytes;
+        // copy-in: the slot is free once the copy-out of chunk c - kSlots has read it;
+        // q, k, v first (the forward's inputs), then dO (the backward's)
         if (c >= kSlots && (e = cudaStreamWaitEvent(ps->copy_in, ps->d2h[s], 0)) != cudaSuccess) return fail(e);
         for (int i = 0; i < 4; ++i) {
             e = cudaMemcpyAsync(t[i], static_cast<const uint8_t *>(in_host[i]) + off, bytes, cudaMemcpyHostToDevice,
                                 ps->copy_in);
             if (e != cudaSuccess) return fail(e);
+            if (i == 2 && (e = cudaEventRecord(ps->h2d_fwd[s], ps->copy_in)) != cudaSuccess) return fail(e);
         }
-        if ((e = cudaEventRecord(ps->h2d[s], ps->copy_in)) != cudaSuccess) return fail(e);
+        if ((e = cudaEventRecord(ps->h2d_bwd[s], ps->copy_in)) != cudaSuccess) return fail(e);
         // kernels: even chunks on the caller's stream, odd chunks on the internal compute
         // stream, so that one chunk's kernels can fill the SMs the other's leave idle
         const cudaStream_t ks = (c & 1) ? ps->compute : cs;
         const fa_stream_t kss = reinterpret_cast<fa_stream_t>(ks);
-        if ((e = cudaStreamWaitEvent(ks, ps->h2d[s], 0)) != cudaSuccess) return fail(e);
+        if ((e = cudaStreamWaitEvent(ks, ps->h2d_fwd[s], 0)) != cudaSuccess) return fail(e);
         st = fa_fwd(t[0], t[1], t[2], t[4], lse_d, 1, n, N, d, scale, causal, kss);
         if (st != FA_OK) return st;
+        if ((e = cudaEventRecord(ps->fwd[s], ks)) != cudaSuccess) return fail(e);
+        if ((e = cudaStreamWaitEvent(ks, ps->h2d_bwd[s], 0)) != cudaSuccess) return fail(e);
         st = fa_bwd(t[0], t[1], t[2], t[4], lse_d, t[3], t[5], t[6], t[7], ws, ws_bytes, 1, n, N, d, scale, causal,
                     kss);
         if (st != FA_OK) return st;
         if ((e = cudaEventRecord(ps->comp[s], ks)) != cudaSuccess) return fail(e);
-        // copy-out
-        if ((e = cudaStreamWaitEvent(ps->copy_out, ps->comp[s], 0)) != cudaSuccess) return fail(e);
-        const int out_idx[4] = {4, 5, 6, 7};
-        for (int i = 0; i < 4; ++i) {
-            e = cudaMemcpyAsync(static_cast<uint8_t *>(out_host[i]) + off, t[out_idx[i]], bytes,
-                                cudaMemcpyDeviceToHost, ps->copy_out);
-            if (e != cudaSuccess) return fail(e);
-        }
-        e = cudaMemcpyAsync(reinterpret_cast<uint8_t *>(lse) + h0 * head_lse, lse_d, n * head_lse,
+        // copy-out: o and lse once the forward is done (the backward only reads o), then
+        // dq, dk, dv
+        if ((e = cudaStreamWaitEvent(ps->copy_out, ps->fwd[s], 0)) != cudaSuccess) return fail(e);
+        e = cudaMemcpyAsync(static_cast<uint8_t *>(o) + off, t[4], bytes, cudaMemcpyDeviceToHost, ps->copy_out);
+        if (e != cudaSuccess) return fail(e);
+        e = cudaMemcpyAsync(reinterpret_cast<uint8_t *>(lse) + static_cast<size_t>(h0) * head_lse, lse_d, n * head_lse,
                             cudaMemcpyDeviceToHost, ps->copy_out);
         if (e != cudaSuccess) return fail(e);
+        if ((e = cudaStreamWaitEvent(ps->copy_out, ps->comp[s], 0)) != cudaSuccess) return fail(e);
+        for (int i = 5; i < 8; ++i) {   // dq dk dv
+            e = cudaMemcpyAsync(static_cast<uint8_t *>(out_host[i - 4]) + off, t[i], bytes, cudaMemcpyDeviceToHost,
+                                ps->copy_out);
+            if (e != cudaSuccess) return fail(e);
+        }
         if ((e = cudaEventRecord(ps->d2h[s], ps->copy_out)) != cudaSuccess) return fail(e);
     }
     // the caller's stream continues once every result is in host memory

@@ -280,7 +280,9 @@ size_t fa_fwd_bwd_host_buffer_size(int B, int H, int N, int d, int chunk_heads);
  * into chunks of chunk_heads consecutive heads; chunk c is copied in on an internal
  * stream, computed on `stream` (even chunks) or an internal compute stream (odd
  * chunks), and copied out on another internal stream, while chunks c - 1 and c + 1
- * are being copied.
+ * are being copied.  Within a chunk the forward starts once q, k and v have landed
+ * (dout follows them), and o and lse are copied out once the forward is done, ahead
+ * of dq, dk and dv.
  *   q, k, v, dout   [B,H,N,d] bf16, HOST memory, read only
  *   o, dq, dk, dv   [B,H,N,d] bf16, HOST memory, written
  *   lse             [B,H,N]   fp32, HOST memory, written

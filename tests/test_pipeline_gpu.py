@@ -59,6 +59,22 @@ def test_host_step_matches_device_step(d, causal, chunk):
             assert torch.equal(g, r), name
 
 
+@pytest.mark.parametrize("chunk", [0, 2])
+def test_host_step_odd_head_count(chunk):
+    """33 heads: the automatic chunk of ceil(33 / 8) = 5 heads leaves a last chunk of 3,
+    chunks of 2 a last chunk of 1; with 11 or 17 chunks every slot of the ring is reused
+    several times.  Each head is computed once, in some chunk."""
+    B, H, N, d = 3, 11, 130, 64
+    q, k, v, do = inputs.random_inputs(B, H, N, d, seed=65, with_grad_out=True)
+    ref = device_step(q, k, v, do, True, 0.125)
+    got = host_step(q, k, v, do, True, 0.125, chunk)
+    for name, g, r in zip(("o", "lse", "dq", "dk", "dv"), got, ref):
+        if name == "dq":
+            assert float((g.float() - r.float()).abs().max()) <= 1e-2 * float(r.float().abs().max())
+        else:
+            assert torch.equal(g, r), name
+
+
 def test_host_step_pageable_memory():
     """Pageable host buffers are correct too (the copies just do not overlap)."""
     B, H, N, d = 1, 4, 200, 128
