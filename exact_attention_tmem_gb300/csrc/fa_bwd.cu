@@ -29,12 +29,14 @@
 // Tensor memory (512 columns): dK [0, d) | dV [d, 2d) | S^T [2d, 2d+128) | dP^T [2d+128,
 // 2d+256).  P^T (bf16) is written over the first 64 S^T columns, and dQ_i accumulates in
 // the dP^T columns once the softmax warps have read dP^T.  Per query block the MMA warp
-// issues dQ_i | dK_i | dP^T_{i+1} (after the dQ_i read-out) | dV_{i+1} | S^T_{i+2}: the
-// read-out gates only the next dP^T.
+// issues dQ_i | dK_i | dP^T_{i+1} (after the dQ_i read-out) | dV_{i+1}, and the S^T
+// warp S^T_{i+2} once Q_{i+2} has landed: the read-out gates only the next dP^T.
 //
-// Warp roles (320 threads): warps 0-3 own one key row each (softmax recompute and dS),
+// Warp roles (352 threads): warps 0-3 own one key row each (softmax recompute and dS),
 // warps 4-7 own one query row each (dQ read-out, staging and bulk reduce), warp 8
-// issues the MMAs, warp 9 issues the TMA loads.  Every wait is time-limited (see
+// issues the MMAs, warp 9 issues the TMA loads, and warp 10 issues the S^T products
+// of the single-pass kernel (the MMA warp issues them in the dK/dV-only kernel, where
+// warp 10 has nothing to do).  Every wait is time-limited (see
 // ptx.cuh).  The shared-memory budget at d = 128 is within 1 KB of the 227 KB limit,
 // so the kernel relies on the dynamic shared window starting 1024-byte aligned and
 // checks it instead of over-allocating (a misaligned start is reported, not used).
@@ -49,6 +51,10 @@ namespace {
 constexpr int kThreads = 320;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
+// The single-pass key-block kernel has an eleventh warp that issues the S^T products
+// (so that the MMA warp never blocks on a Q tile while dS_i is ready).
+constexpr int kSWarp = 10;
+constexpr int kMainThreads = 352;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // kDQ = false (the dK/dV-only kernel) needs neither the dS tile nor the dQ staging
@@ -77,7 +83,7 @@ struct BwdCfg {
     static constexpr int kLOff = kDQOff + kDQStageBytes;
     static constexpr int kDOff = kLOff + kVecStages * kVecBytes;
     static constexpr int kBarOff = kDOff + kVecStages * kVecBytes;
-    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + kVecStages + 7;
+    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + kVecStages + 9;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16;
     // tensor memory
@@ -110,6 +116,8 @@ struct BwdBars {
     static constexpr int kDQFull = kSFull + 4;
     static constexpr int kDQFree = kSFull + 5;
     static constexpr int kDrain = kSFull + 6;
+    static constexpr int kDVIssued = kSFull + 7;   // dV_i handed to the tensor pipe (S^T_{i+1} may follow)
+    static constexpr int kSDrain = kSFull + 8;     // the S^T warp's products have completed
 };
 
 enum : int {
@@ -200,7 +208,7 @@ bwd_post_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq
 // dV only (dQ comes from bwd_dq_kernel); per query block the MMA warp then issues
 // dV_i | S^T_{i+1} | dK_i | dP^T_{i+1}, and dS is not staged in shared memory.
 template <int D, bool kDQ>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kMainThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_dq, const float *__restrict__ lse2,
@@ -260,6 +268,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(bar(B::kDQFull), 1);
         mbar_init(bar(B::kDQFree), 128);
         mbar_init(bar(B::kDrain), 1);
+        mbar_init(bar(B::kDVIssued), 1);
+        mbar_init(bar(B::kSDrain), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -378,13 +388,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             bool ok = mbar_wait_w(bar(B::kKV), 0, kSiteBMmaKV);
             tc_fence_after();
             int qs = -1, dos = -1;
-            if (ok) {
-                qs = wait_q(0);
-                ok = qs >= 0;
+            if constexpr (!kDQ) {   // single pass: the S^T products come from the S^T warp
+                if (ok) {
+                    qs = wait_q(0);
+                    ok = qs >= 0;
+                }
+                if (ok) {
+                    mma_kk(tS, sK, sQ + qs * C::kTileBytes);
+                    umma_commit(bar(B::kSFull));
+                }
             }
             if (ok) {
-                mma_kk(tS, sK, sQ + qs * C::kTileBytes);
-                umma_commit(bar(B::kSFull));
                 dos = wait_do(0);
                 ok = dos >= 0;
             }
@@ -396,24 +410,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // dS_i is in shared memory only (the dS^T tile read K-major is dK's A
                 // operand, read MN-major it is dQ's), so dQ_i goes first, into the dP^T
                 // columns the softmax warps have finished reading.  Per query block:
-                // dQ_i | dK_i | dP^T_{i+1} (after the dQ_i read-out) | dV_{i+1} |
-                // S^T_{i+2}: the chain from dS_i to dS_{i+1} is dQ, dK, the read-out and
-                // dP^T; dK_i completes before dP^T_{i+1}, so the softmax warps overwrite
-                // the dS tile only after both products have read it.
-                if (ok) {  // dV_0, then S^T_1
+                // dQ_i | dK_i | dP^T_{i+1} (after the dQ_i read-out) | dV_{i+1}, and the
+                // S^T warp adds S^T_{i+2} once Q_{i+2} has landed and dV_{i+1} (which
+                // reads P^T_{i+1} from the S^T columns) is in the pipe ahead of it.  The
+                // chain from dS_i to dS_{i+1} is dQ, dK, the read-out and dP^T; dK_i
+                // completes before dP^T_{i+1}, so the softmax warps overwrite the dS tile
+                // only after both products have read it.
+                if (ok) {  // dV_0
                     ok = mbar_wait_w(bar(B::kPFull), 0, kSiteBMmaP);
                     if (ok) {
                         tc_fence_after();
                         mma_tn(tDV, tS, sDO + dos * C::kTileBytes, false);
                         umma_commit(bar(B::kDOEmpty + dos));     // dP^T_0 and dV_0 have read dO_0
-                    }
-                    if (ok && n_it > 1) {
-                        const int qn = wait_q(1);
-                        ok = qn >= 0;
-                        if (ok) {
-                            mma_kk(tS, sK, sQ + qn * C::kTileBytes);
-                            umma_commit(bar(B::kSFull));
-                        }
+                        if (lane == 0) mbar_arrive(bar(B::kDVIssued));
                     }
                 }
                 for (int it = 0; ok && it < n_it; ++it) {
@@ -461,12 +470,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         tc_fence_after();
                         mma_tn(tDV, tS, sDO + dn * C::kTileBytes, true);
                         umma_commit(bar(B::kDOEmpty + dn));
-                        if (it + 2 < n_it) {  // S^T_{i+2}: P^T_{i+1} is read by dV_{i+1} first
-                            const int qn = wait_q(it + 2);
-                            if (qn < 0) { ok = false; break; }
-                            mma_kk(tS, sK, sQ + qn * C::kTileBytes);
-                            umma_commit(bar(B::kSFull));
-                        }
+                        if (lane == 0) mbar_arrive(bar(B::kDVIssued));
                     }
                 }
             } else {
@@ -499,6 +503,45 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // epilogue waits on the same commit (it follows the last dK product).
             umma_commit(bar(B::kDrain));
             mbar_wait_drain(bar(B::kDrain), 0, wc, kSiteBDrain);
+        }
+    } else if (warp == kSWarp) {
+        // ------------------------------------------------------------ S^T issuer (single pass)
+        // S^T_i = K_j Q_i^T once Q_i has landed and dV_{i-1} has been issued: the
+        // product overwrites the S^T columns that dV_{i-1} reads, and the tensor pipe
+        // runs products in the order they were issued.  The whole warp runs the loop;
+        // lane 0 issues.
+        if constexpr (kDQ) {
+            auto wait_w = [&](uint32_t b, uint32_t parity, int site) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
+            };
+            const uint32_t tS = tmem + C::kSCol;
+            bool ok = wait_w(bar(B::kKV), 0, kSiteBMmaKV);
+            int issued = 0;
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int qs = it % C::kQStages;
+                if (!wait_w(bar(B::kQFull + qs), (it / C::kQStages) & 1, kSiteBMmaQ)) { ok = false; break; }
+                if (it > 0 && !wait_w(bar(B::kDVIssued), (it - 1) & 1, kSiteBMmaP)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t a0 = sdesc_sw128(sK, 16, 1024);
+                const uint64_t b0 = sdesc_sw128(sQ + qs * C::kTileBytes, 16, 1024);
+                uint64_t a[C::kKSteps], b[C::kKSteps];
+#pragma unroll
+                for (int kk = 0; kk < C::kKSteps; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kBoxTileBytes + (kk & 3) * 32;
+                    a[kk] = sdesc_step(a0, off);
+                    b[kk] = sdesc_step(b0, off);
+                }
+                if constexpr (C::kKSteps == 8) umma_f16_ss_x8(tS, a, b, C::kIdescSS, 0u);
+                else umma_f16_ss_x4(tS, a, b, C::kIdescSS, 0u);
+                umma_commit(bar(B::kSFull));
+                ++issued;
+            }
+            // tensor memory is released after the final barrier: let this warp's
+            // products finish first (they normally have long before)
+            if (issued > 0) {
+                umma_commit(bar(B::kSDrain));
+                mbar_wait_drain(bar(B::kSDrain), 0, wc, kSiteBDrain);
+            }
         }
     } else if (warp < 4) {
         // ------------------------------------------------------------ key rows: P^T and dS^T
@@ -1104,7 +1147,7 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
     const long long blocks = static_cast<long long>(a.BH / a.group) * nkv;
     if (blocks <= 0 || blocks > INT_MAX) return cudaErrorInvalidValue;
     const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-    kern<<<static_cast<unsigned>(blocks), kThreads, smem_bytes, stream>>>(
+    kern<<<static_cast<unsigned>(blocks), kMainThreads, smem_bytes, stream>>>(
         a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.lse2, a.delta, static_cast<__nv_bfloat16 *>(a.dk),
         static_cast<__nv_bfloat16 *>(a.dv), a.N, a.Npad, nkv, a.group, a.scale, scale_log2, a.causal, a.status);
     e = cudaGetLastError();
