@@ -227,8 +227,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t sK = base + C::kKOff, sV = base + C::kVOff, sQ = base + C::kQOff;
     const uint32_t sDO = base + C::kDOOff, sDS = base + C::kDSOff, sDQ = base + C::kDQOff;
     const uint32_t sL = base + C::kLOff, sD = base + C::kDOff, sBar = base + C::kBarOff;
-    const float *Lvec = reinterpret_cast<const float *>(smem + C::kLOff);
-    const float *Dvec = reinterpret_cast<const float *>(smem + C::kDOff);
     uint8_t *dS_ptr = smem + C::kDSOff;
     uint8_t *dQ_stage = smem + C::kDQOff;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
@@ -568,24 +566,33 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             {
                 uint32_t sr[128];
                 tmem_ld_x128(tSr, sr);
-                const float2 *nL = reinterpret_cast<const float2 *>(Lvec + vs * kTileRows);  // -L * log2 e
+                const uint32_t nL = sL + vs * C::kVecBytes;   // -L * log2 e, 4 queries per load
                 const float2 sl2 = make_float2(scale_log2, scale_log2);
                 // causal: query q sees key c iff c <= q (same block offsets on the diagonal)
                 const int qmin = (causal && i == j) ? c : 0;
                 if (key_valid && qmin == 0) {
 #pragma unroll
-                    for (int u = 0; u < 64; ++u) {
-                        const float2 x = fma2(make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])),
-                                              sl2, nL[u]);
-                        pk[u] = pack_bf16(ex2(x.x), ex2(x.y));
+                    for (int u = 0; u < 64; u += 2) {
+                        const float4 l4 = lds_f4(nL + 8 * u);
+                        const float2 x0 = fma2(make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])),
+                                               sl2, make_float2(l4.x, l4.y));
+                        const float2 x1 = fma2(make_float2(__uint_as_float(sr[2 * u + 2]), __uint_as_float(sr[2 * u + 3])),
+                                               sl2, make_float2(l4.z, l4.w));
+                        pk[u] = pack_bf16(ex2(x0.x), ex2(x0.y));
+                        pk[u + 1] = pack_bf16(ex2(x1.x), ex2(x1.y));
                     }
                 } else {
 #pragma unroll
-                    for (int u = 0; u < 64; ++u) {
-                        const float2 x = fma2(make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])),
-                                              sl2, nL[u]);
-                        pk[u] = pack_bf16((key_valid && 2 * u >= qmin) ? ex2(x.x) : 0.f,
-                                          (key_valid && 2 * u + 1 >= qmin) ? ex2(x.y) : 0.f);
+                    for (int u = 0; u < 64; u += 2) {
+                        const float4 l4 = lds_f4(nL + 8 * u);
+                        const float2 x0 = fma2(make_float2(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])),
+                                               sl2, make_float2(l4.x, l4.y));
+                        const float2 x1 = fma2(make_float2(__uint_as_float(sr[2 * u + 2]), __uint_as_float(sr[2 * u + 3])),
+                                               sl2, make_float2(l4.z, l4.w));
+                        pk[u] = pack_bf16((key_valid && 2 * u >= qmin) ? ex2(x0.x) : 0.f,
+                                          (key_valid && 2 * u + 1 >= qmin) ? ex2(x0.y) : 0.f);
+                        pk[u + 1] = pack_bf16((key_valid && 2 * u + 2 >= qmin) ? ex2(x1.x) : 0.f,
+                                              (key_valid && 2 * u + 3 >= qmin) ? ex2(x1.y) : 0.f);
                     }
                 }
             }
@@ -596,7 +603,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDPFull), it & 1, wc, kSiteBSoftDP));
             if (!ok) break;
             tc_fence_after();
-            const float2 *D2 = reinterpret_cast<const float2 *>(Dvec + vs * kTileRows);
+            const uint32_t sDv = sD + vs * C::kVecBytes;   // D, 4 queries per load
             // 32 query columns at a time; the load of the next chunk is in flight while
             // this chunk is computed and stored
             uint32_t rbuf[2][32];
@@ -608,12 +615,18 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (ch < 3) tmem_ld_x32_nowait(tDPr + 32u * (ch + 1), rbuf[(ch + 1) & 1]);
                 uint32_t dk2[16];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const uint32_t pp = pk[16 * ch + t];
-                    const float2 p = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u));
-                    const float2 ds = mul2(p, sub2(make_float2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1])),
-                                                   D2[16 * ch + t]));
-                    dk2[t] = pack_bf16(ds.x, ds.y);
+                for (int t = 0; t < 16; t += 2) {
+                    const float4 d4 = lds_f4(sDv + 4 * (32 * ch + 2 * t));
+                    const uint32_t pp0 = pk[16 * ch + t], pp1 = pk[16 * ch + t + 1];
+                    const float2 p0 = make_float2(__uint_as_float(pp0 << 16), __uint_as_float(pp0 & 0xffff0000u));
+                    const float2 p1 = make_float2(__uint_as_float(pp1 << 16), __uint_as_float(pp1 & 0xffff0000u));
+                    const float2 ds0 = mul2(p0, sub2(make_float2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1])),
+                                                     make_float2(d4.x, d4.y)));
+                    const float2 ds1 = mul2(p1, sub2(make_float2(__uint_as_float(r[2 * t + 2]),
+                                                                 __uint_as_float(r[2 * t + 3])),
+                                                     make_float2(d4.z, d4.w)));
+                    dk2[t] = pack_bf16(ds0.x, ds0.y);
+                    dk2[t + 1] = pack_bf16(ds1.x, ds1.y);
                 }
                 // shared: query columns 32*ch .. 32*ch+31 = box (ch / 2), 16-byte chunks
                 // 4*(ch % 2) .. 4*(ch % 2)+3 of this key's row (read by the dQ and dK products)

@@ -495,6 +495,14 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
+// Four fp32 values from shared memory (16-byte aligned shared-window address).  The asm
+// is volatile so that it stays after the barrier wait that made the data visible.
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
 // ---------------------------------------------------------------------------------
 // small math helpers
 // ---------------------------------------------------------------------------------
