@@ -43,9 +43,9 @@ REF_STEP_ROWS = 32      # query rows per head per step of the reference arm
 # they had when the counters were taken; after any change it reads as null until the
 # capture is repeated.
 TRAFFIC = {
-    "bwd": (2016.2e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "44e2e97555ae2ac6"),
-    "bwd_det": (1660.0e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "44e2e97555ae2ac6"),
-    "fwd": (491.4e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "0c0439e89c78474f"),
+    "bwd": (2010.1e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "0f76f9f560f0e67d"),
+    "bwd_det": (1661.5e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "0f76f9f560f0e67d"),
+    "fwd": (491.9e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "bcee718484425fc2"),
 }
 
 
@@ -631,17 +631,21 @@ def run_e2e(args, world, dev, stream, host_in, causal, scale, flops):
                         buffer=buf, chunk_heads=chunk)
 
     e2e_steps = max(1, min(args.steps, 5))
-    e2e_step()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
+    for _ in range(2):   # warm-up: first use of the pinned buffers and of the library's streams
         e2e_step()
-    e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    # one event pair per step, back to back on the stream: the sum is the whole span
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+    ev[0].record(stream)
+    for i in range(e2e_steps):
+        e2e_step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(e2e_steps)]
+    e2e_ms = max_over_ranks(sum(step_ms), dev) / e2e_steps
     return {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+            "step_ms": [round(t, 3) for t in step_ms],
             "path": f"fa_fwd_bwd_host, pinned host buffers, chunks of {chunk} heads"}
 
 
