@@ -48,13 +48,15 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
+// Both tiled kernels: warp 8 issues the MMAs, warp 9 the TMA loads.  The key-block
+// kernel (bwd_main_kernel) has an eleventh warp that issues the S^T products of the
+// single-pass variant, so that the MMA warp never blocks on a Q tile while dS_i is
+// ready; the query-block kernel (bwd_dq_kernel) has ten warps.
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
-// The single-pass key-block kernel has an eleventh warp that issues the S^T products
-// (so that the MMA warp never blocks on a Q tile while dS_i is ready).
 constexpr int kSWarp = 10;
 constexpr int kMainThreads = 352;
+constexpr int kDqThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // kDQ = false (the dK/dV-only kernel) needs neither the dS tile nor the dQ staging
@@ -816,7 +818,7 @@ enum : int {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const float *__restrict__ lse2, const float *__restrict__ delta, __nv_bfloat16 *__restrict__ dq,
@@ -1174,7 +1176,7 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
         const int num_pairs = (nkv + 1) / 2;
         const long long qblocks = static_cast<long long>(a.BH) * num_pairs;
         if (qblocks > INT_MAX) return cudaErrorInvalidValue;
-        qkern<<<static_cast<unsigned>(qblocks), kThreads, CQ::kSmemBytes, stream>>>(
+        qkern<<<static_cast<unsigned>(qblocks), kDqThreads, CQ::kSmemBytes, stream>>>(
             a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, static_cast<__nv_bfloat16 *>(a.dq), a.N, a.Npad,
             num_pairs, a.group, a.scale, scale_log2, a.causal, a.status);
         return cudaGetLastError();
