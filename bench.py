@@ -43,9 +43,9 @@ REF_STEP_ROWS = 32      # query rows per head per step of the reference arm
 # they had when the counters were taken; after any change it reads as null until the
 # capture is repeated.
 TRAFFIC = {
-    "bwd": (2010.1e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "b82f1a9a4e041f0d"),
-    "bwd_det": (1661.5e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "b82f1a9a4e041f0d"),
-    "fwd": (491.9e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "bcee718484425fc2"),
+    "bwd": (2010.1e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "dc943c9ac1da5c6f"),
+    "bwd_det": (1661.5e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "dc943c9ac1da5c6f"),
+    "fwd": (491.9e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "30b0c1032f610325"),
 }
 
 

@@ -183,10 +183,6 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *map, uint32
         : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until the shared-memory sources of every committed bulk group have been read.
-__device__ __forceinline__ void bulk_wait_group_read0() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 // Waits until the sources of all but the most recently committed bulk group have been read.
 __device__ __forceinline__ void bulk_wait_group_read1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -282,45 +278,8 @@ constexpr uint32_t kFormatTF32 = 2;
 constexpr uint32_t kFormatE4M3 = 0;   // kind::f8f6f4 operand format
 
 // ---------------------------------------------------------------------------------
-// tcgen05: MMA issue (one thread) and commit
+// tcgen05: MMA issue (lane 0 of the calling warp) and commit
 // ---------------------------------------------------------------------------------
-template <bool kTF32>
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-    if constexpr (kTF32) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-            : "memory");
-    }
-}
-
-// A operand from tensor memory (M rows in lanes, K along columns), B from shared memory.
-template <bool kTF32>
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-    if constexpr (kTF32) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-            : "memory");
-    }
-}
-
 // Warp-collective forms: the whole warp executes the call (so descriptors and
 // addresses stay warp-uniform and the issuing code stays short) and lane 0 alone
 // issues the instruction.  The commit must come from the same lane as the MMAs.
@@ -416,19 +375,6 @@ __device__ __forceinline__ void umma_f16_ts_x8(uint32_t d_tmem, uint32_t a_tmem,
         : "memory");
 }
 
-__device__ __forceinline__ void umma_f16_ts_x4(uint32_t d_tmem, uint32_t a_tmem, const uint64_t (&b)[4],
-                                                uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, t, e;\n\t.reg .b32 l, ta;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
-        "setp.ne.b32 p, %3, 0;\n\tsetp.eq.u32 t, l, l;\n\t"
-        "add.u32 ta, %1, 0;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %4, %2, p;\n\t"
-        "add.u32 ta, %1, 8;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %5, %2, t;\n\t"
-        "add.u32 ta, %1, 16;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %6, %2, t;\n\t"
-        "add.u32 ta, %1, 24;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %7, %2, t;\n\t"
-        "}"
-        ::"r"(d_tmem), "r"(a_tmem), "r"(idesc), "r"(accumulate), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
-        : "memory");
-}
 __device__ __forceinline__ void umma_f8_ss_x4(uint32_t d_tmem, const uint64_t (&a)[4], const uint64_t (&b)[4],
                                                 uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -462,37 +408,11 @@ __device__ __forceinline__ uint64_t sdesc_step(uint64_t desc, uint32_t bytes) {
     return (desc & 0xFFFFFFFF00000000ull) | static_cast<uint32_t>(static_cast<uint32_t>(desc) + (bytes >> 4));
 }
 
-// kind::f8f6f4 (8-bit A and B, fp32 accumulator), warp-collective like umma_ss/umma_ts.
-__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
         : "memory");
-}
-
-// The mbarrier receives one arrival when every tcgen05 operation issued so far by
-// this thread has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
 }
 
 // Four fp32 values from shared memory (16-byte aligned shared-window address).  The asm
@@ -607,21 +527,6 @@ __device__ __forceinline__ void tmem_ld_x128(uint32_t taddr, uint32_t (&r)[128])
         : "r"(taddr)
         : "memory");
 }
-
-// tcgen05.st, shape 32x32b, 32 repetitions, without waiting: the source registers are
-// read at issue; call tmem_wait_st() before signalling that tensor memory is ready.
-__device__ __forceinline__ void tmem_st_x32_nowait(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-        "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
-        :
-        : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-          "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-          "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // tcgen05.st, shape 32x32b, 32 repetitions (the mirror of tmem_ld_x32); waits for completion.
 __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
