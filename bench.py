@@ -37,9 +37,11 @@ E2E_CHUNK_HEADS = 8     # heads per chunk of the host-buffer pipeline (e2e)
 REF_STEP_ROWS = 32      # query rows per head per step of the reference arm
 
 
-# DRAM bytes (read + write) per call of the bench shape, from the ncu capture summarised
-# in profiles/dram_traffic_fwd_bwd_B1_H32_N8192_d128_causal.md (half the heads, scaled
-# by 2).  A figure is reported only while the kernel sources still hash to the value
+# DRAM bytes (read + write) per call of the bench shape, from one ncu capture of
+# dram__bytes_read.sum + dram__bytes_write.sum over every launch of the attention kernels
+# (`ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
+# -k "regex:fwd_kernel|bwd_" python bench.py --shape 1,32,8192,128 --steps 1 --warmup 3
+# --no-cpu-baseline --no-e2e`: half the heads of the bench shape, scaled by 2).  A figure is reported only while the kernel sources still hash to the value
 # they had when the counters were taken; after any change it reads as null until the
 # capture is repeated.
 TRAFFIC = {

@@ -16,7 +16,8 @@
 // Set-up: the first call on each device, with that device current, looks up the
 // array's device address with cudaGetSymbolAddress (the array's name in host code is
 // only a host-side stand-in, not a device address) and caches it per device.  That
-// first call should therefore come before any stream capture.
+// first call should therefore come before any stream capture.  The stream must belong
+// to the current device (checked; another device's stream is an argument error).
 //
 // Sharing: every call uses the same array, and the array keeps the previous call's
 // contents.  The backward's pre-processing kernel rewrites every part of the workspace
@@ -78,6 +79,12 @@ extern "C" int fa_bwd_noalloc(const void *q, const void *k, const void *v, const
     if (need == 0)  // invalid or unsupported shape: fa_bwd reports which, before using a workspace
         return fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, nullptr, 0, B, H, N, d, scale, causal, stream);
     if (need > kScratchBytes) return FA_ERR_WORKSPACE;
+    // The array used is the current device's: a stream of another device would run the
+    // kernels there against this device's address.
+    int cur = 0, sdev = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaStreamGetDevice(reinterpret_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) return FA_ERR_CUDA;
+    if (sdev != cur) return FA_ERR_INVALID_ARG;
     void *scratch = nullptr;
     const int st = scratch_for_current_device(&scratch);
     if (st != FA_OK) return st;

@@ -87,7 +87,13 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
 /*
  * Forward pass with float32 inputs and outputs (same layout and meaning as
  * fa_fwd; q, k, v, o are float32).  The two products run on the tensor cores
- * in TF32 with fp32 accumulation.  Supported for d = 64 only.
+ * in TF32 with fp32 accumulation.  Supported for d = 64 only (the fp32 workload:
+ * one head, N = 256, d = 64, non-causal).
+ * Page: "FlashAttention" (deep dive), section "How it works" (the same forward loop:
+ * running max m and sum l, O = acc / l, L = m + log l) and its section "Code" (the
+ * tiled loop on fp32 slices, one head, row-major N x d, checked against naive softmax
+ * attention); tile sizes change only the summation order ("Flash Attention and
+ * Memory-Efficient Attention Variants", active recall A3).
  */
 int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,
                int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
@@ -97,6 +103,10 @@ int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *
  * dQ accumulator plus two fp32 per-row vectors (D = rowsum(dO o O) and the
  * logsumexp in base 2), padded to whole 128-row tiles.  Returns 0 if the
  * arguments are invalid.
+ * Page: "FlashAttention" (deep dive), section "How it works" (the backward pass
+ * uses D = rowsum(dO o O) per query row and recomputes P from the saved L) and
+ * section "Pitfalls" (dQ gathers contributions from every key block: summed across
+ * thread blocks into one fp32 accumulator per element, which is this workspace).
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -256,6 +266,8 @@ int fa_fwd_fp8(const void *q8, const void *k8, const void *vt8, const float *des
  *   The first call on a device looks up the array's device address (with that device
  *   current); make that first call before any stream capture.  All calls share the
  *   array, so calls whose kernels overlap on the GPU (e.g. on two streams) race.
+ *   `stream` must belong to the current device: the array used is the current
+ *   device's, and a stream of another device is rejected with FA_ERR_INVALID_ARG.
  *   Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  */
 int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse,
@@ -306,6 +318,11 @@ int fa_fwd_bwd_host(const void *q, const void *k, const void *v, const void *dou
                     fa_stream_t stream);
 
 /*
+ * Error reporting.  The pages fix no error convention ("FlashAttention" deep dive,
+ * section "Pitfalls", lists what to guard against: fully masked rows, 32-bit offset
+ * overflow, head dims the tensor cores cannot take); the status codes above and the
+ * three calls below are this library's own.
+ *
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT if a kernel gave up
  * waiting since the last call (its outputs are then undefined).  Returns
@@ -322,10 +339,12 @@ int fa_get_device_status(fa_stream_t stream);
  */
 int fa_selftest_wait_timeout(fa_stream_t stream);
 
-/* Static, human-readable name of a status code (never NULL). */
+/* Static, human-readable name of a status code (never NULL).  The pages define no
+ * error convention: the names are this library's own. */
 const char *fa_status_string(int status);
 
-/* The cudaError_t of the last call that returned FA_ERR_CUDA in this thread. */
+/* The cudaError_t of the last call that returned FA_ERR_CUDA in this thread (the
+ * pages define no error convention: this library's own). */
 int fa_last_cuda_error(void);
 
 #ifdef __cplusplus

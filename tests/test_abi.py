@@ -332,3 +332,26 @@ def test_fwd_bwd_host_valid_call_without_gpu_reports_cuda_error(lib):
         pytest.skip("a GPU is present")
     assert host_step(lib) == _lib.FA_ERR_CUDA
     assert _lib.last_cuda_error() != 0
+
+
+def _largest_n_within(lib, limit, B, H, d):
+    """The largest N whose fa_bwd workspace fits in `limit` bytes (binary search)."""
+    lo, hi = 1, 1 << 24
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if lib.fa_bwd_workspace_size(B, H, mid, d) <= limit:
+            lo = mid
+        else:
+            hi = mid - 1
+    return lo
+
+
+@pytest.mark.parametrize("B,H,d", [(1, 4, 128), (2, 3, 64)])
+def test_noalloc_limit_is_exact(lib, B, H, d):
+    """fa_bwd_noalloc takes every problem whose workspace fits its built-in array and
+    rejects, on the host before any launch, the next size up."""
+    limit = _lib.NOALLOC_SCRATCH_BYTES
+    n = _largest_n_within(lib, limit, B, H, d)
+    assert lib.fa_bwd_workspace_size(B, H, n, d) <= limit < lib.fa_bwd_workspace_size(B, H, n + 1, d)
+    st = lib.fa_bwd_noalloc(*([A] * 9), B, H, n + 1, d, ctypes.c_float(0.1), 1, None)
+    assert st == _lib.FA_ERR_WORKSPACE

@@ -123,3 +123,21 @@ def test_workload4_backward_eight_heads():
     ref = oracle.attention_bwd(sub(q), sub(k), sub(v), sub(do), w.scale, True)
     for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         assert_grad_close(g[sel_b, sel_h][None], r, name, f"workload 4 heads {heads}")
+
+
+@pytest.mark.slow
+def test_default_bwd_benchmarked_shape():
+    """B=2 H=32 N=8192 d=128 causal, the benchmarked problem, through fa_bwd (the
+    single-pass route the benchmark times: dQ summed with bulk reductions); three seeded
+    (batch, head) pairs checked in full against the oracle."""
+    w = inputs.WORKLOADS[3]
+    q, k, v, do = inputs.workload_inputs(3, with_grad_out=True)
+    dq, dk, dv = gpu_fwd_bwd(q, k, v, do, True, w.scale)
+    heads = [(0, 0), (1, 31), (1, 7)]
+    sel_b = [b for b, _ in heads]
+    sel_h = [h for _, h in heads]
+    f = inputs.as_f64
+    sub = lambda t: f(t)[sel_b, sel_h][None]
+    ref = oracle.attention_bwd(sub(q), sub(k), sub(v), sub(do), w.scale, True)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert_grad_close(g[sel_b, sel_h][None], r, name, f"workload 3 heads {heads}")

@@ -7,6 +7,7 @@ whatever the launch holds, so o, lse, dk and dv must equal the device path bit f
 dQ is summed with reductions whose order varies, so it is compared within a tolerance."""
 import math
 
+import numpy as np
 import pytest
 import torch
 
@@ -122,3 +123,28 @@ def test_host_step_waits_for_earlier_work_on_the_stream():
             assert float((g.float() - r.float()).abs().max()) <= 1e-2 * float(r.float().abs().max())
         else:
             assert torch.equal(g, r), name
+
+
+@pytest.mark.slow
+def test_host_step_benchmarked_shape_against_oracle():
+    """The end-to-end call the benchmark times: B=2 H=32 N=8192 d=128 causal on host
+    buffers in chunks of 8 heads; o and lse on three seeded heads in full and 256 sampled
+    rows of every head, the gradients of the same three heads in full, against the oracle."""
+    w = inputs.WORKLOADS[3]
+    q, k, v, do = inputs.workload_inputs(3, with_grad_out=True)
+    o, lse, dq, dk, dv = host_step(q, k, v, do, True, w.scale, chunk=8)
+    f = inputs.as_f64
+    heads = [(0, 0), (1, 31), (1, 7)]
+    sel_b = [b for b, _ in heads]
+    sel_h = [h for _, h in heads]
+    sub = lambda t: f(t)[sel_b, sel_h][None]
+    o_ref, l_ref = oracle.attention_fwd(sub(q), sub(k), sub(v), w.scale, True)
+    assert_fwd_close(o.double().numpy()[sel_b, sel_h][None], lse.double().numpy()[sel_b, sel_h][None],
+                     o_ref, l_ref, f"host step, workload 3 heads {heads}")
+    rows = inputs.sample_rows(w.N, 256, seed=3303)
+    o_s, l_s = oracle.attention_fwd_rows(f(q), f(k), f(v), w.scale, True, rows)
+    assert_fwd_close(o.double().numpy()[:, :, rows], lse.double().numpy()[:, :, rows], o_s, l_s,
+                     "host step, workload 3 sampled rows")
+    ref = oracle.attention_bwd(sub(q), sub(k), sub(v), sub(do), w.scale, True)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert_grad_close(g.double().numpy()[sel_b, sel_h][None], r, name, f"host step, workload 3 heads {heads}")

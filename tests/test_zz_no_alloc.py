@@ -46,6 +46,38 @@ def test_noalloc_backward_matches_fa_bwd_twice(d, causal):
                               f"no-alloc call {call + 1}, d={d}, causal={causal}")
 
 
+def test_noalloc_backward_near_the_scratch_limit():
+    """A problem whose workspace fills the built-in array to within one 128-row tile
+    (the per-row vectors sit past the dQ accumulator, at the top of the array): the
+    results match fa_bwd with a caller-owned workspace."""
+    import exact_attention_tmem_gb300 as fa
+    fa.build()
+    lib = _lib.load()
+    B, H, d = 1, 4, 128
+    limit = _lib.NOALLOC_SCRATCH_BYTES
+    lo, hi = 1, 1 << 20
+    while lo < hi:                      # the largest N whose workspace fits
+        mid = (lo + hi + 1) // 2
+        if lib.fa_bwd_workspace_size(B, H, mid, d) <= limit:
+            lo = mid
+        else:
+            hi = mid - 1
+    N = lo
+    need = lib.fa_bwd_workspace_size(B, H, N, d)
+    assert limit - 128 * (B * H) * (d * 4 + 8) < need <= limit
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = to_dev(*inputs.random_inputs(B, H, N, d, seed=919, with_grad_out=True))
+    o, lse = fa.fwd(q, k, v, causal=True, scale=scale)
+    ref = fa.bwd(q, k, v, o, lse, do, causal=True, scale=scale)
+    for call in range(2):
+        got = _noalloc_bwd(q, k, v, o, lse, do, True, scale)
+        torch.cuda.synchronize()
+        assert fa.device_status() == 0
+        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+        assert_grad_close(got[0].float().cpu().numpy(), ref[0].float().cpu().numpy(), "dQ",
+                          f"no-alloc near the limit (N={N}), call {call + 1}")
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     lib = _lib.load()
     B, H, N, d = 8, 16, 4096, 128       # needs ~260 MB of scratch
