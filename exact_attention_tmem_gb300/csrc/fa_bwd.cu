@@ -136,43 +136,63 @@ __global__ void __launch_bounds__(256)
 bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
                const float *__restrict__ lse, float *__restrict__ delta, float *__restrict__ lse2,
                float *__restrict__ dq_acc, int N, int Npad, int BH) {
+    // The main kernel is launched as this grid's dependent: it may start its set-up (and
+    // its loads of Q, K, V, dO) as soon as every CTA of this grid is running, and waits
+    // for this grid's results before it reads D, L or the accumulator.
+    grid_launch_dependents();
     constexpr int kLanesPerRow = D / 8;              // 16-byte chunks per row
     constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+    constexpr int kUnroll = 4;                       // row groups in flight per warp
     const int lane = threadIdx.x & 31;
     const int sub = lane / kLanesPerRow;
     const int part = lane % kLanesPerRow;
     const long long warp_global = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
     const long long total_rows = static_cast<long long>(BH) * Npad;
-    for (long long base = warp_global * kRowsPerWarp; base < total_rows; base += nwarps * kRowsPerWarp) {
-        const long long r = base + sub;
-        float acc = 0.f;
-        bool valid = false;
-        long long src_row = 0;
-        if (r < total_rows) {
-            const long long bh = r / Npad;
-            const int i = static_cast<int>(r % Npad);
-            valid = i < N;
-            src_row = bh * N + i;
-            if (valid) {
-                const uint4 a = reinterpret_cast<const uint4 *>(o + src_row * D)[part];
-                const uint4 b = reinterpret_cast<const uint4 *>(dout + src_row * D)[part];
-                const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
-                const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+    for (long long base = warp_global * kRowsPerWarp * kUnroll; base < total_rows;
+         base += nwarps * kRowsPerWarp * kUnroll) {
+        // all loads of the group first, then the sums
+        uint4 a[kUnroll], b[kUnroll];
+        float lv[kUnroll];
+        bool valid[kUnroll];
+        long long rr[kUnroll];
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float2 fa = __bfloat1622float2(pa[t]);
-                    const float2 fb = __bfloat1622float2(pb[t]);
-                    acc = fmaf(fa.x, fb.x, acc);
-                    acc = fmaf(fa.y, fb.y, acc);
+        for (int u = 0; u < kUnroll; ++u) {
+            rr[u] = base + u * kRowsPerWarp + sub;
+            valid[u] = false;
+            a[u] = make_uint4(0u, 0u, 0u, 0u);
+            b[u] = a[u];
+            lv[u] = 0.f;
+            if (rr[u] < total_rows) {
+                const long long bh = rr[u] / Npad;
+                const int i = static_cast<int>(rr[u] - bh * Npad);
+                valid[u] = i < N;
+                if (valid[u]) {
+                    const long long src_row = bh * N + i;
+                    a[u] = reinterpret_cast<const uint4 *>(o + src_row * D)[part];
+                    b[u] = reinterpret_cast<const uint4 *>(dout + src_row * D)[part];
+                    if (part == 0) lv[u] = lse[src_row];
                 }
             }
         }
 #pragma unroll
-        for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (r < total_rows && part == 0) {
-            delta[r] = valid ? acc : 0.f;
-            lse2[r] = valid ? -lse[src_row] * kLog2e : -INFINITY;
+        for (int u = 0; u < kUnroll; ++u) {
+            float acc = 0.f;
+            const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a[u]);
+            const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b[u]);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float2 fa = __bfloat1622float2(pa[t]);
+                const float2 fb = __bfloat1622float2(pb[t]);
+                acc = fmaf(fa.x, fb.x, acc);
+                acc = fmaf(fa.y, fb.y, acc);
+            }
+#pragma unroll
+            for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (rr[u] < total_rows && part == 0) {
+                delta[rr[u]] = valid[u] ? acc : 0.f;
+                lse2[rr[u]] = valid[u] ? -lv[u] * kLog2e : -INFINITY;
+            }
         }
     }
     if (dq_acc == nullptr) return;   // the deterministic backward has no accumulator
@@ -188,6 +208,7 @@ bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restr
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
 bwd_post_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq, long long n8, float scale) {
+    grid_dependency_wait();   // launched as the main kernel's dependent: its reductions are in
     const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
     const float4 *src = reinterpret_cast<const float4 *>(dq_acc);
@@ -314,6 +335,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const int r = it - C::kVecStages;
                     if (!mbar_wait(bar(B::kQEmpty + r % C::kQStages), (r / C::kQStages) & 1, wc, kSiteBLoadQ)) break;
                 }
+                // D and L come from the pre-processing grid (this kernel may have started before it
+                // finished): wait for that grid before the first vector load
+                if (it == 0) grid_dependency_wait();
                 mbar_arrive_expect_tx(bar(B::kVecFull + vs), 2 * C::kVecBytes);
                 bulk_load(sL + vs * C::kVecBytes, lrow + i * kTileRows, C::kVecBytes, bar(B::kVecFull + vs));
                 bulk_load(sD + vs * C::kVecBytes, drow + i * kTileRows, C::kVecBytes, bar(B::kVecFull + vs));
@@ -688,6 +712,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t tDQr = tmem + lane_off + C::kDPCol;  // dQ_i accumulates in the dP^T columns
         bool ok = true;
         int g = 0;   // dQ boxes issued so far
+        // the accumulator is cleared by the pre-processing grid: wait for it before reducing
+        if (kDQ && threadIdx.x == 128) grid_dependency_wait();
         for (int it = 0; kDQ && it < n_it; ++it) {
             const int i = q_block(it);
             // all 128 threads leave together, so none is left waiting at a named barrier
@@ -1162,10 +1188,22 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
     const long long blocks = static_cast<long long>(a.BH / a.group) * nkv;
     if (blocks <= 0 || blocks > INT_MAX) return cudaErrorInvalidValue;
     const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-    kern<<<static_cast<unsigned>(blocks), kMainThreads, smem_bytes, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.lse2, a.delta, static_cast<__nv_bfloat16 *>(a.dk),
-        static_cast<__nv_bfloat16 *>(a.dv), a.N, a.Npad, nkv, a.group, a.scale, scale_log2, a.causal, a.status);
-    e = cudaGetLastError();
+    // programmatic dependent launch: the main kernel's set-up overlaps the end of the
+    // pre-processing grid (it waits for that grid's results before using them)
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kMainThreads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, static_cast<const float *>(a.lse2),
+                           static_cast<const float *>(a.delta), static_cast<__nv_bfloat16 *>(a.dk),
+                           static_cast<__nv_bfloat16 *>(a.dv), a.N, a.Npad, nkv, a.group, a.scale, scale_log2,
+                           a.causal, a.status);
     if (e != cudaSuccess) return e;
 
     if (a.deterministic) {
@@ -1183,9 +1221,14 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t stream) {
     }
 
     const long long n8 = static_cast<long long>(a.BH) * a.N * D / 8;
-    bwd_post_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(a.dq_acc, static_cast<__nv_bfloat16 *>(a.dq), n8,
-                                                           a.scale);
-    return cudaGetLastError();
+    cudaLaunchConfig_t pcfg = {};
+    pcfg.gridDim = dim3(static_cast<unsigned>(grid_for(n8, 256)));
+    pcfg.blockDim = dim3(256);
+    pcfg.stream = stream;
+    pcfg.attrs = pdl;
+    pcfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&pcfg, bwd_post_kernel, static_cast<const float *>(a.dq_acc),
+                              static_cast<__nv_bfloat16 *>(a.dq), n8, a.scale);
 }
 
 }  // namespace

@@ -55,14 +55,30 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 // start first, so the last CTAs of the grid are short ones (no long tail on a few
 // SMs), while the group's heads alone are in flight and their tiles stay in L2.
 constexpr int kHeadGroup = 8;
-__device__ __forceinline__ void heavy_first_order(int idx, int per_head, int &head, int &rank) {
-    const int num_heads = static_cast<int>(gridDim.x) / per_head;
+__host__ __device__ __forceinline__ void heavy_first_item(int idx, int per_head, int num_heads, int &head,
+                                                          int &rank) {
     const int per_group = kHeadGroup * per_head;
     const int g = idx / per_group;
     const int r = idx - g * per_group;
-    const int heads_here = min(kHeadGroup, num_heads - g * kHeadGroup);
+    const int rest = num_heads - g * kHeadGroup;
+    const int heads_here = rest < kHeadGroup ? rest : kHeadGroup;
     rank = r / heads_here;
     head = g * kHeadGroup + r % heads_here;
+}
+// The same order for a grid of exactly num_heads x per_head CTAs, one item each.
+__device__ __forceinline__ void heavy_first_order(int idx, int per_head, int &head, int &rank) {
+    heavy_first_item(idx, per_head, static_cast<int>(gridDim.x) / per_head, head, rank);
+}
+
+// ---------------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------------
+// Waits for the grids this one depends on (programmatic dependent launch); a no-op for
+// a normal launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets a grid launched after this one with programmatic serialization start now.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------------
