@@ -77,6 +77,7 @@ decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
                     float *__restrict__ part_acc, int Nk, int chunk_keys, int num_chunks, int max_chunks,
                     int group, float scale_log2, unsigned int *status) {
     using C = DecCfg<D, G>;
+    grid_launch_dependents();   // the merge kernel may launch now; it waits for this grid
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t base = smem_u32(smem);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff);
@@ -308,6 +309,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                   float *__restrict__ part_acc, int Nk, int chunk_keys, int num_chunks, int max_chunks, int group,
                   float scale_log2, unsigned int *status) {
     using C = DecMmaCfg<D>;
+    grid_launch_dependents();   // the merge kernel may launch now; it waits for this grid
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;     // 128-byte swizzle repeats every 1 KB
@@ -511,6 +513,7 @@ __global__ void __launch_bounds__(D)
 decode_combine_kernel(const float *__restrict__ part_m, const float *__restrict__ part_l,
                       const float *__restrict__ part_acc, __nv_bfloat16 *__restrict__ o, float *__restrict__ lse,
                       int num_chunks, int max_chunks) {
+    grid_dependency_wait();     // launched as the split kernel's dependent: its partials are in
     const int bh = blockIdx.x;
     const int e = threadIdx.x;
     const int64_t base = static_cast<int64_t>(bh) * max_chunks;
@@ -530,6 +533,25 @@ decode_combine_kernel(const float *__restrict__ part_m, const float *__restrict_
     if (e == 0) lse[bh] = (M + __log2f(L)) * kDecLn2;
 }
 
+// The merge of the chunks' triples, launched as the split kernel's programmatic
+// dependent: its CTAs can be scheduled once every split CTA is running (during the split
+// grid's last wave) and start merging the moment that grid completes.
+template <int D>
+cudaError_t launch_combine(const DecodeArgs &a, cudaStream_t stream) {
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.BHkv * a.group));
+    cfg.blockDim = dim3(D);
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, static_cast<const float *>(a.part_m),
+                              static_cast<const float *>(a.part_l), static_cast<const float *>(a.part_acc),
+                              static_cast<__nv_bfloat16 *>(a.o), a.lse, a.num_chunks, a.max_chunks);
+}
+
 template <int D, int G>
 cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
     using C = DecCfg<D, G>;
@@ -545,9 +567,7 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream) {
         a.max_chunks, a.group, scale_log2, a.status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<D><<<static_cast<unsigned>(a.BHkv * a.group), D, 0, stream>>>(
-        a.part_m, a.part_l, a.part_acc, static_cast<__nv_bfloat16 *>(a.o), a.lse, a.num_chunks, a.max_chunks);
-    return cudaGetLastError();
+    return launch_combine<D>(a, stream);
 }
 
 template <int D>
@@ -564,9 +584,7 @@ cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t stream) {
         a.chunk_keys, a.num_chunks, a.max_chunks, a.group, scale_log2, a.status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<D><<<static_cast<unsigned>(a.BHkv * a.group), D, 0, stream>>>(
-        a.part_m, a.part_l, a.part_acc, static_cast<__nv_bfloat16 *>(a.o), a.lse, a.num_chunks, a.max_chunks);
-    return cudaGetLastError();
+    return launch_combine<D>(a, stream);
 }
 
 template <int D>
