@@ -45,9 +45,9 @@ REF_STEP_ROWS = 32      # query rows per head per step of the reference arm
 # they had when the counters were taken; after any change it reads as null until the
 # capture is repeated.
 TRAFFIC = {
-    "bwd": (2010.1e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "dc943c9ac1da5c6f"),
-    "bwd_det": (1661.5e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "dc943c9ac1da5c6f"),
-    "fwd": (491.9e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "30b0c1032f610325"),
+    "bwd": (2016.6e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "91c4aba07ff647ea"),
+    "bwd_det": (1661.0e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "91c4aba07ff647ea"),
+    "fwd": (492.8e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "a3607ab5b76c9b18"),
 }
 
 
