@@ -197,7 +197,7 @@ def decode_workspace_size(B: int, H: int, Hkv: int, Nk: int, d: int) -> int:
 
 def decode(q, k, v, scale: float | None = None, out=None, lse=None, workspace=None, num_chunks: int = 0):
     """One query row per head against all keys: q [B, H, d], k and v [B, Hkv, Nk, d]
-    (bf16, Hkv dividing H, H / Hkv <= 8).  Returns (o [B, H, d] bf16, lse [B, H] fp32).
+    (bf16, Hkv dividing H, H / Hkv <= 16).  Returns (o [B, H, d] bf16, lse [B, H] fp32).
     The keys are split into chunks merged on the device (num_chunks = 0: automatic)."""
     if q.dim() != 3 or k.dim() != 4:
         raise ValueError("expected q [B, H, d] and k, v [B, Hkv, Nk, d]")

@@ -119,3 +119,24 @@ def test_decode_workload_sampled_heads():
                                              f(v[b:b + 1, kv:kv + 1]), 1.0 / math.sqrt(d))
         assert float(np.abs(o[b, h].float().cpu().numpy() - O_ref[0, 0]).max()) <= TOL_O
         assert abs(float(lse[b, h]) - L_ref[0, 0]) <= TOL_L
+
+
+def test_decode_back_to_back_calls_share_a_workspace():
+    """Two decoding calls enqueued back to back with one workspace and different inputs:
+    the second call's split kernel writes the triples the first call's merge kernel
+    (a dependent launch) reads; stream order must keep them apart.  Each result equals
+    the same call made alone, bit for bit."""
+    import exact_attention_tmem_gb300 as fa
+    B, H, Hkv, Nk, d = 2, 16, 2, 3000, 128
+    a = to_dev(*_inputs(B, H, Hkv, Nk, d, 15100))
+    b = to_dev(*_inputs(B, H, Hkv, Nk, d, 15200))
+    ws = torch.empty(fa.decode_workspace_size(B, H, Hkv, Nk, d), dtype=torch.uint8, device="cuda")
+    alone = []
+    for t in (a, b):
+        alone.append(fa.decode(*t, workspace=ws))
+        torch.cuda.synchronize()
+    together = [fa.decode(*t, workspace=ws) for t in (a, b)]
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    for x, y in zip(alone, together):
+        assert torch.equal(x[0], y[0]) and torch.equal(x[1], y[1])
