@@ -307,7 +307,6 @@ namespace fa {
 namespace {
 // Decoding: key chunks are whole 64-key stages; at most kDecodeMaxChunks per head.
 constexpr int kDecodeChunkAlign = 64;
-constexpr int kDecodeMaxChunks = 256;
 
 int decode_max_chunks(int Nk) {
     const int stages = (Nk + kDecodeChunkAlign - 1) / kDecodeChunkAlign;

@@ -508,25 +508,66 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     }
 }
 
+// One CTA of D threads per (batch, query head); thread e owns output column e.  The
+// merge is latency-bound (a few KB per head), so every load it needs is issued before
+// any arithmetic: the chunks' m and l (one chunk per thread) and thread e's
+// accumulator column of the first kCombinePre chunks.  The sums run in chunk order,
+// as a plain sequential merge would.
+constexpr int kCombinePre = 32;
 template <int D>
 __global__ void __launch_bounds__(D)
 decode_combine_kernel(const float *__restrict__ part_m, const float *__restrict__ part_l,
                       const float *__restrict__ part_acc, __nv_bfloat16 *__restrict__ o, float *__restrict__ lse,
                       int num_chunks, int max_chunks) {
+    constexpr int kPer = kDecodeMaxChunks / D;   // chunks per thread for m and l
+    constexpr int kWarps = D / 32;
+    __shared__ float m_sh[kDecodeMaxChunks], l_sh[kDecodeMaxChunks];
+    __shared__ float red[kWarps];
     grid_dependency_wait();     // launched as the split kernel's dependent: its partials are in
     const int bh = blockIdx.x;
     const int e = threadIdx.x;
     const int64_t base = static_cast<int64_t>(bh) * max_chunks;
-    float M = -INFINITY;
-#pragma unroll 8
-    for (int c = 0; c < num_chunks; ++c) M = fmaxf(M, part_m[base + c]);
+    float a[kCombinePre];
+#pragma unroll
+    for (int j = 0; j < kCombinePre; ++j) a[j] = j < num_chunks ? part_acc[(base + j) * D + e] : 0.f;
+    float mv[kPer], lv[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int c = e + j * D;
+        mv[j] = c < num_chunks ? part_m[base + c] : -INFINITY;
+        lv[j] = c < num_chunks ? part_l[base + c] : 0.f;
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int c = e + j * D;
+        if (c < num_chunks) {
+            m_sh[c] = mv[j];
+            l_sh[c] = lv[j];
+        }
+        mx = fmaxf(mx, mv[j]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if ((e & 31) == 0) red[e >> 5] = mx;
+    __syncthreads();
+    float M = red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red[w]);
     float L = 0.f, A = 0.f;
-    // unrolled so that the chunks' loads are in flight together
-#pragma unroll 8
-    for (int c = 0; c < num_chunks; ++c) {
-        const float mc = part_m[base + c];
+#pragma unroll
+    for (int c = 0; c < kCombinePre; ++c) {
+        if (c < num_chunks) {
+            const float mc = m_sh[c];
+            const float wgt = mc == -INFINITY ? 0.f : ex2(mc - M);   // chunks that saw no key weigh 0
+            L = fmaf(l_sh[c], wgt, L);
+            A = fmaf(a[c], wgt, A);
+        }
+    }
+    for (int c = kCombinePre; c < num_chunks; ++c) {
+        const float mc = m_sh[c];
         const float wgt = mc == -INFINITY ? 0.f : ex2(mc - M);
-        L = fmaf(part_l[base + c], wgt, L);
+        L = fmaf(l_sh[c], wgt, L);
         A = fmaf(part_acc[(base + c) * D + e], wgt, A);
     }
     o[static_cast<int64_t>(bh) * D + e] = __float2bfloat16_rn(A / L);

@@ -42,6 +42,7 @@ struct BwdArgs {
 constexpr int kDecodeBoxRows = 64;    // keys per stage of the tensor-core decoding kernel
 constexpr int kDecodeMmaMinGroup = 2; // query heads per key/value head from which decoding uses it
 constexpr int kDecodeMaxGroup = 16;   // the tensor-core kernel's M dimension
+constexpr int kDecodeMaxChunks = 256; // key chunks per head at most (the merge kernel's table)
 
 // Decoding: one query row per head ([B*H, d]) against K, V [B*Hkv, Nk, d]; the keys of
 // each key/value head are split into num_chunks chunks of chunk_keys keys (a multiple
