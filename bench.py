@@ -66,9 +66,9 @@ L2_NOTE = "L2 flushed between timed calls (256 MiB write, then a 256 MiB read: n
 # they had when the counters were taken; after any change it reads as null until the
 # capture is repeated.
 TRAFFIC = {
-    "bwd": (2016.6e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "91c4aba07ff647ea"),
-    "bwd_det": (1661.0e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "91c4aba07ff647ea"),
-    "fwd": (492.8e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "a3607ab5b76c9b18"),
+    "bwd": (2019.0e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "6a428f4ecc6d6a08"),
+    "bwd_det": (1661.2e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "6a428f4ecc6d6a08"),
+    "fwd": (492.4e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "eba468388e7d0d69"),
 }
 
 
