@@ -85,7 +85,7 @@ struct BwdCfg {
     static constexpr int kLOff = kDQOff + kDQStageBytes;
     static constexpr int kDOff = kLOff + kVecStages * kVecBytes;
     static constexpr int kBarOff = kDOff + kVecStages * kVecBytes;
-    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + kVecStages + 9;
+    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + kVecStages + 10;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16;
     // tensor memory
@@ -120,6 +120,7 @@ struct BwdBars {
     static constexpr int kDrain = kSFull + 6;
     static constexpr int kDVIssued = kSFull + 7;   // dV_i handed to the tensor pipe (S^T_{i+1} may follow)
     static constexpr int kSDrain = kSFull + 8;     // the S^T warp's products have completed
+    static constexpr int kDVDone = kSFull + 9;     // the last dV product has completed
 };
 
 enum : int {
@@ -291,6 +292,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(bar(B::kDrain), 1);
         mbar_init(bar(B::kDVIssued), 1);
         mbar_init(bar(B::kSDrain), 1);
+        mbar_init(bar(B::kDVDone), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -446,6 +448,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         tc_fence_after();
                         mma_tn(tDV, tS, sDO + dos * C::kTileBytes, false);
                         umma_commit(bar(B::kDOEmpty + dos));     // dP^T_0 and dV_0 have read dO_0
+                        if (n_it == 1) umma_commit(bar(B::kDVDone));
                         if (lane == 0) mbar_arrive(bar(B::kDVIssued));
                     }
                 }
@@ -494,6 +497,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         tc_fence_after();
                         mma_tn(tDV, tS, sDO + dn * C::kTileBytes, true);
                         umma_commit(bar(B::kDOEmpty + dn));
+                        if (it + 2 == n_it) umma_commit(bar(B::kDVDone));
                         if (lane == 0) mbar_arrive(bar(B::kDVIssued));
                     }
                 }
@@ -503,6 +507,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tc_fence_after();
                     mma_tn(tDV, tS, sDO + dos * C::kTileBytes, it > 0);
                     umma_commit(bar(B::kDOEmpty + dos));
+                    if (it + 1 == n_it) umma_commit(bar(B::kDVDone));
                     int qs_next = -1;
                     if (it + 1 < n_it) {  // S^T_{i+1}: the S^T columns are free after dV_i
                         qs_next = wait_q(it + 1);
@@ -683,8 +688,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_arrive(bar(B::kDSFull));
         }
         // ------------------------------------------------------------ epilogue: dV row
+        // dV is final once the last dV product has completed (dQ and dK of the last query
+        // block may still be running)
         if (ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDrain), 0, wc, kSiteBEpi));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDVDone), 0, wc, kSiteBEpi));
         }
         if (ok) {
             tc_fence_after();
@@ -748,7 +755,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             }
         }
-        if (threadIdx.x == 128) bulk_wait_group0();
+        // the staging buffers must have been read before the CTA releases its shared memory
+        if (threadIdx.x == 128) bulk_wait_group_read0();
         // ------------------------------------------------------------ epilogue: dK row
         if (ok) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B::kDrain), 0, wc, kSiteBEpi));

@@ -203,8 +203,12 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 __device__ __forceinline__ void bulk_wait_group_read1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
-// Waits until every committed bulk group has completed (global writes performed).
-__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Waits until the sources of every committed bulk group have been read: the shared
+// memory may then be reused or released.  The global writes complete on their own and
+// are visible to any grid that waits for this one to finish.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // Barrier over `count` threads (a multiple of 32) with hardware barrier `id` (1..15).
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
