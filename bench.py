@@ -672,6 +672,65 @@ def run_e2e(args, world, dev, stream, host_in, causal, scale, flops):
             "path": f"fa_fwd_bwd_host, pinned host buffers, chunks of {chunk} heads"}
 
 
+def run_link(args, world, rank, local):
+    """Host-link bandwidth for the end-to-end step's bytes (pinned host memory): the step's
+    inputs host->device alone, its outputs device->host alone, and both at once on two
+    streams.  The last is the floor for ``e2e``: every byte has to cross the link."""
+    import torch
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B, H, N, d = args.shape or (2, 32, 8192, 128)
+    n_in = 4 * B * H * N * d * 2                   # q, k, v, dO (bf16)
+    n_out = 4 * B * H * N * d * 2 + B * H * N * 4  # o, dq, dk, dv (bf16) and L (fp32)
+    hin = torch.empty(n_in, dtype=torch.uint8).pin_memory()
+    hout = torch.empty(n_out, dtype=torch.uint8).pin_memory()
+    din = torch.empty(n_in, dtype=torch.uint8, device=dev)
+    dout = torch.empty(n_out, dtype=torch.uint8, device=dev)
+    cur = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def copies(up, down):
+        s_in.wait_stream(cur)
+        s_out.wait_stream(cur)
+        if up:
+            with torch.cuda.stream(s_in):
+                din.copy_(hin, non_blocking=True)
+        if down:
+            with torch.cuda.stream(s_out):
+                hout.copy_(dout, non_blocking=True)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
+
+    res = {}
+    for name, up, down in (("h2d", True, False), ("d2h", False, True), ("both", True, True)):
+        for _ in range(args.warmup):
+            copies(up, down)
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cur)
+            copies(up, down)
+            e1.record(cur)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        res[name] = statistics.median(ts)
+    if rank != 0:
+        return
+    line = {
+        "metric": "host link bandwidth, pinned host memory, the bench step's bytes", "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "config": {"workload": f"fwd+bwd B={B} H={H} N={N} d={d}: inputs in, outputs out",
+                   "bytes_in": n_in, "bytes_out": n_out},
+        "h2d_gbs": n_in / (res["h2d"] * 1e-3) / 1e9, "d2h_gbs": n_out / (res["d2h"] * 1e-3) / 1e9,
+        "both_gbs": (n_in + n_out) / (res["both"] * 1e-3) / 1e9,
+        "h2d_ms": res["h2d"], "d2h_ms": res["d2h"], "both_ms": res["both"],
+        "e2e_floor_ms": res["both"],
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -688,6 +747,8 @@ def main():
                     help="time the decoding kernel (one query row per head) instead of the fwd+bwd step")
     ap.add_argument("--decode-shape", type=lambda x: tuple(int(v) for v in x.split(",")), default=None,
                     metavar="B,H,Hkv,Nk,d", help="decode workload (default 8,32,32,32768,128)")
+    ap.add_argument("--link", action="store_true",
+                    help="measure the host link for the end-to-end step's bytes instead")
     ap.add_argument("--deterministic", action="store_true",
                     help="time the deterministic backward (fa_bwd_deterministic) in the step")
     ap.add_argument("--shape", type=lambda x: tuple(int(v) for v in x.split(",")), default=None,
@@ -702,7 +763,9 @@ def main():
         run_reference(args, world, rank)
     else:
         world, rank, local = dist_setup("nccl")
-        if args.decode:
+        if args.link:
+            run_link(args, world, rank, local)
+        elif args.decode:
             run_decode(args, world, rank, local)
         elif args.fp8:
             run_fp8(args, world, rank, local)
