@@ -66,9 +66,9 @@ L2_NOTE = "L2 flushed between timed calls (256 MiB write, then a 256 MiB read: n
 # they had when the counters were taken; after any change it reads as null until the
 # capture is repeated.
 TRAFFIC = {
-    "bwd": (2019.0e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "6a428f4ecc6d6a08"),
-    "bwd_det": (1661.2e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "6a428f4ecc6d6a08"),
-    "fwd": (492.4e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "eba468388e7d0d69"),
+    "bwd": (2020.0e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "35d5dace122f5144"),
+    "bwd_det": (1662.8e6, ('fa_bwd.cu', 'fa_api.cu', 'ptx.cuh', 'fa_internal.h'), "35d5dace122f5144"),
+    "fwd": (492.8e6, ('fa_fwd.cu', 'ptx.cuh', 'fa_internal.h'), "6c55da67cfcceb0d"),
 }
 
 
