@@ -685,6 +685,9 @@ cudaError_t decode_ctas_per_sm(int d, int group, int *out) {
 }
 
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t stream) {
+    // the merge keeps one table entry per chunk in shared memory (checked before any launch)
+    if (a.num_chunks < 1 || a.num_chunks > kDecodeMaxChunks || a.num_chunks > a.max_chunks)
+        return cudaErrorInvalidValue;
     if (a.d == 64) return launch_decode_d<64>(a, stream);
     if (a.d == 128) return launch_decode_d<128>(a, stream);
     return cudaErrorInvalidValue;

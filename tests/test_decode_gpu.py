@@ -67,6 +67,15 @@ def test_decode_chunk_counts(chunks):
     _check(q, k, v, 1.0 / math.sqrt(d), f"chunks={chunks}", chunks=chunks)
 
 
+@pytest.mark.parametrize("Hkv,d", [(4, 64), (1, 128)])
+def test_decode_most_chunks(Hkv, d):
+    """The largest chunk count the workspace holds (256 chunks of one 64-key stage): every
+    slot of the merge's per-chunk table is used."""
+    B, H, Nk = 1, 4, 256 * 64
+    q, k, v = _inputs(B, H, Hkv, Nk, d, seed=13500 + Hkv + d)
+    _check(q, k, v, 1.0 / math.sqrt(d), f"256 chunks Hkv={Hkv} d={d}", chunks=256)
+
+
 def test_decode_peaked_scores():
     """Scores spread over hundreds of units: the per-stage and cross-chunk rescales."""
     B, H, Hkv, Nk, d = 1, 4, 4, 5000, 128
