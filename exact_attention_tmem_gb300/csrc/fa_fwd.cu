@@ -37,7 +37,6 @@ namespace fa {
 namespace {
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr float kRescaleBound = 256.0f;    // 2^kRescaleThreshold
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <typename T, int D, int QT>
@@ -392,23 +391,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             // mask: causal (key > query) and keys past N in the last tile
             const int kv0 = j * kTileRows;
             const int lim = min(causal ? row_g - kv0 : kTileRows - 1, N - 1 - kv0);
-            // The whole row is loaded up front except on the bf16 fast path of the
-            // one-tile-per-CTA variant, which streams S from tensor memory in chunks
-            // (exp_pass_tmem; measured on GB300: non-causal N=8192 1383 -> 1458 TFLOP/s,
-            // while the two-tile causal variant ran slower that way, 1486 -> 1388).
-            constexpr bool kStream = !C::kTF32 && QT == 1 && D == 128;
-            const bool whole_row = !kStream || __any_sync(0xffffffffu, m_run == -INFINITY);
+            // the whole row of S in registers, masked
             uint32_t sr[128];
-            auto apply_mask = [&]() {
-                if (lim < kTileRows - 1) {
+            tmem_ld_x128(tSr, sr);
+            if (lim < kTileRows - 1) {
 #pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (c > lim) sr[c] = __float_as_uint(-INFINITY);
-                }
-            };
-            if (whole_row) {
-                tmem_ld_x128(tSr, sr);
-                apply_mask();
+                for (int c = 0; c < 128; ++c)
+                    if (c > lim) sr[c] = __float_as_uint(-INFINITY);
             }
             // Row max of the scaled scores (base-2 units): four chains of three-input max.
             auto row_max = [&]() -> float {
@@ -466,87 +455,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     const float2 accs = add2(acc0, acc1);
                     return accs.x + accs.y;
                 };
-                // The same pass reading S from tensor memory 32 columns at a time, the load
-                // of the next chunk in flight while the current chunk is exponentiated.
-                auto exp_pass_tmem = [&](float m) -> float {
-                    const float neg = (m == -INFINITY) ? 0.f : -m;
-                    const float2 ng2 = make_float2(neg, neg);
-                    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-                    uint32_t rb[2][32];
-                    tmem_ld_x32_nowait(tSr, rb[0]);
-                    tmem_wait_ld_fence(rb[0]);
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        if (ch < 3) tmem_ld_x32_nowait(tSr + 32u * (ch + 1), rb[(ch + 1) & 1]);
-                        uint32_t(&r)[32] = rb[ch & 1];
-                        if (lim < kTileRows - 1) {
-#pragma unroll
-                            for (int c = 0; c < 32; ++c)
-                                if (32 * ch + c > lim) r[c] = __float_as_uint(-INFINITY);
-                        }
-#pragma unroll
-                        for (int u = 0; u < 16; ++u) {
-                            const float2 x =
-                                fma2(make_float2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), sl2, ng2);
-                            const float2 p = make_float2(ex2(x.x), ex2(x.y));
-                            if (u & 1) acc1 = add2(acc1, p); else acc0 = add2(acc0, p);
-                            pk[16 * ch + u] = pack_bf16(p.x, p.y);
-                        }
-                        if (ch < 3) tmem_wait_ld_fence(rb[(ch + 1) & 1]);
-                    }
-                    const float2 accs = add2(acc0, acc1);
-                    return accs.x + accs.y;
-                };
-                // Fast path: exponentiate against the running max.  A block sum below 2^8
-                // means every P is below 2^8, the bound the lazy rescale allows, so the
-                // row max is not needed.  Otherwise take the max (reading S again from
-                // tensor memory, where it still is) and recompute only if it grew by more
-                // than the threshold.  The first block always starts from the max.
-                float blk;
-                if (whole_row) {
-                    // max first (the first block of every row; kept warp-uniform)
-                    const float mx = row_max();
-                    upd = mx > m_run + (m_run == -INFINITY ? 0.f : kRescaleThreshold);
-                    if (upd) {
-                        alpha = ex2(m_run - mx);
-                        m_run = mx;
-                    }
-                    blk = exp_pass(m_run);
-                } else {
-                    blk = kStream ? exp_pass_tmem(m_run) : exp_pass(m_run);
-                    // tcgen05.ld is warp-collective: the slow path is taken by the whole
-                    // warp when any of its rows needs it.
-                    if (__any_sync(0xffffffffu, !(blk < kRescaleBound))) {
-                        float m4 = -INFINITY;
-#pragma unroll
-                        for (int ch = 0; ch < 4; ++ch) {
-                            uint32_t r[32];
-                            tmem_ld_x32(tSr + 32u * ch, r);
-                            float a0 = -INFINITY, a1 = -INFINITY;
-#pragma unroll
-                            for (int c = 0; c < 32; c += 4) {
-                                const int cc = 32 * ch + c;
-                                a0 = max3(a0, cc > lim ? -INFINITY : __uint_as_float(r[c]),
-                                          cc + 1 > lim ? -INFINITY : __uint_as_float(r[c + 1]));
-                                a1 = max3(a1, cc + 2 > lim ? -INFINITY : __uint_as_float(r[c + 2]),
-                                          cc + 3 > lim ? -INFINITY : __uint_as_float(r[c + 3]));
-                            }
-                            m4 = max3(m4, a0, a1);
-                        }
-                        const float mx = m4 * scale_log2;
-                        upd = mx > m_run + kRescaleThreshold;
-                        if (upd) {
-                            alpha = ex2(m_run - mx);
-                            m_run = mx;
-                        }
-                        // Rows whose max did not move recompute exactly the P they had.
-                        if (__any_sync(0xffffffffu, upd)) {
-                            tmem_ld_x128(tSr, sr);
-                            apply_mask();
-                            blk = exp_pass(m_run);
-                        }
-                    }
+                // The row max first; the running max moves (and O is rescaled) only when the
+                // row max exceeds it by more than the threshold (lazy rescale).
+                const float mx = row_max();
+                upd = mx > m_run + (m_run == -INFINITY ? 0.f : kRescaleThreshold);
+                if (upd) {
+                    alpha = ex2(m_run - mx);
+                    m_run = mx;
                 }
+                const float blk = exp_pass(m_run);
                 tmem_st_x64(tSr, pk);
                 sum0 = blk;
                 sum1 = 0.f;
@@ -639,12 +556,15 @@ cudaError_t launch_fwd_t(const FwdArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// bf16 tile policy (measured on GB300): causal work is best served by two query tiles
-// per CTA (the pair 2g, 2g+1 has nearly equal cost); non-causal by one tile per CTA and
-// two CTAs per SM, which gives each tile its own MMA-issuing thread.
+// bf16 tile policy (measured on GB300): two query tiles per CTA (for causal work the
+// pair 2g, 2g+1 has nearly equal cost), except non-causal work at d = 64, where one tile
+// per CTA and two CTAs per SM (each tile with its own MMA-issuing thread) is faster.
 template <int D>
 cudaError_t launch_fwd_bf16_d(const FwdArgs &a, cudaStream_t stream) {
-    return a.causal ? launch_fwd_t<__nv_bfloat16, D, 2>(a, stream) : launch_fwd_t<__nv_bfloat16, D, 1>(a, stream);
+    if constexpr (D == 64) {
+        if (!a.causal) return launch_fwd_t<__nv_bfloat16, D, 1>(a, stream);
+    }
+    return launch_fwd_t<__nv_bfloat16, D, 2>(a, stream);
 }
 
 }  // namespace
