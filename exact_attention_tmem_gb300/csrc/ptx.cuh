@@ -50,20 +50,25 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 // launch order of attention work items
 // ---------------------------------------------------------------------------------
 // A grid of num_heads x per_head CTAs, where rank 0 of a head is its longest walk
-// (causal work) is taken in groups of kHeadGroup heads, rank-major inside a group:
-// rank 0 of every head of the group, then rank 1, ...  The longest walks of a group
-// start first, so the last CTAs of the grid are short ones (no long tail on a few
-// SMs), while the group's heads alone are in flight and their tiles stay in L2.
-constexpr int kHeadGroup = 8;
+// (causal work) is taken in groups of heads, rank-major inside a group: rank 0 of every
+// head of the group, then rank 1, ...  The longest walks of a group start first, so the
+// last CTAs of the grid are short ones (no long tail on a few SMs), while the group's
+// heads alone are in flight and their tiles stay in L2.  A group has 8 heads, or more
+// when a head has few work items, so that it holds at least 128 CTAs.
+__host__ __device__ __forceinline__ int heavy_first_group(int per_head) {
+    const int g = (128 + per_head - 1) / per_head;
+    return g > 8 ? g : 8;
+}
 __host__ __device__ __forceinline__ void heavy_first_item(int idx, int per_head, int num_heads, int &head,
                                                           int &rank) {
-    const int per_group = kHeadGroup * per_head;
+    const int group = heavy_first_group(per_head);
+    const int per_group = group * per_head;
     const int g = idx / per_group;
     const int r = idx - g * per_group;
-    const int rest = num_heads - g * kHeadGroup;
-    const int heads_here = rest < kHeadGroup ? rest : kHeadGroup;
+    const int rest = num_heads - g * group;
+    const int heads_here = rest < group ? rest : group;
     rank = r / heads_here;
-    head = g * kHeadGroup + r % heads_here;
+    head = g * group + r % heads_here;
 }
 // The same order for a grid of exactly num_heads x per_head CTAs, one item each.
 __device__ __forceinline__ void heavy_first_order(int idx, int per_head, int &head, int &rank) {
