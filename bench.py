@@ -33,7 +33,7 @@ WORKLOAD_ID = 3      # B=2 H=32 N=8192 d=128 causal, bf16
 CAUSAL = True
 L2_FLUSH_BYTES = 256 << 20
 CPU_SAMPLE_ROWS = 256   # query rows per head timed on the host for cpu_baseline
-E2E_CHUNK_HEADS = 8     # heads per chunk of the host-buffer pipeline (e2e)
+E2E_CHUNK_HEADS = 4     # heads per chunk of the host-buffer pipeline (e2e)
 REF_STEP_ROWS = 32      # query rows per head per step of the reference arm
 
 

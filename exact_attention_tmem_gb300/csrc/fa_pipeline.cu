@@ -59,7 +59,7 @@ bool slot_layout(int hc, int N, int d, SlotLayout *L) {
 }
 
 int resolve_chunk(int BH, int chunk_heads) {
-    if (chunk_heads <= 0) chunk_heads = (BH + 7) / 8;   // about eight chunks
+    if (chunk_heads <= 0) chunk_heads = (BH + 15) / 16;   // about sixteen chunks
     return chunk_heads > BH ? BH : chunk_heads;
 }
 

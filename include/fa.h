@@ -278,7 +278,7 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
  * Bytes of device buffer fa_fwd_bwd_host needs: three slots, each holding one chunk
  * of chunk_heads heads (q, k, v, dout, o, dq, dk, dv in bf16, lse in fp32, and the
  * chunk's fa_bwd workspace), each part 256-byte aligned.  chunk_heads <= 0 picks
- * ceil(B*H / 8); a value above B*H is clamped to B*H.  Returns 0 if the arguments
+ * ceil(B*H / 16); a value above B*H is clamped to B*H.  Returns 0 if the arguments
  * are invalid.
  */
 size_t fa_fwd_bwd_host_buffer_size(int B, int H, int N, int d, int chunk_heads);

@@ -128,11 +128,12 @@ def test_host_step_waits_for_earlier_work_on_the_stream():
 @pytest.mark.slow
 def test_host_step_benchmarked_shape_against_oracle():
     """The end-to-end call the benchmark times: B=2 H=32 N=8192 d=128 causal on host
-    buffers in chunks of 8 heads; o and lse on three seeded heads in full and 256 sampled
+    buffers in chunks of 4 heads; o and lse on three seeded heads in full and 256 sampled
     rows of every head, the gradients of the same three heads in full, against the oracle."""
+    import bench
     w = inputs.WORKLOADS[3]
     q, k, v, do = inputs.workload_inputs(3, with_grad_out=True)
-    o, lse, dq, dk, dv = host_step(q, k, v, do, True, w.scale, chunk=8)
+    o, lse, dq, dk, dv = host_step(q, k, v, do, True, w.scale, chunk=bench.E2E_CHUNK_HEADS)
     f = inputs.as_f64
     heads = [(0, 0), (1, 31), (1, 7)]
     sel_b = [b for b, _ in heads]
